@@ -1,0 +1,376 @@
+"""Pins of the CPU oracle against things other than itself: values the pages print for worked
+examples, library routines (torch / numpy on CPU), closed forms, invariants and brute force."""
+import itertools
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _from_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+
+
+# ------------------------------------------------------------------------------------ bf16
+def test_bf16_matches_torch_on_float_inputs():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        [0.0, -0.0, 1.0, -1.0, 3.0e38, 1e-40, -1e-41]]).astype(np.float32)
+    ours = oracle.bf16_from_double(v.astype(np.float64))
+    ref = _bf16_bits(torch.from_numpy(v))
+    np.testing.assert_array_equal(ours, ref)
+    np.testing.assert_array_equal(oracle.bf16_to_double(ours), _from_bits(ref).to(torch.float64).numpy())
+
+
+def test_bf16_ties_and_single_rounding_from_double():
+    cases = {
+        1.0: 0x3F80,
+        1.0 + 2.0 ** -8: 0x3F80,  # midpoint 1 | 1+2^-7: tie to even (down)
+        1.0 + 3 * 2.0 ** -8: 0x3F82,  # midpoint 1+2^-7 | 1+2^-6: tie to even (up)
+        1.0 + 2.0 ** -8 + 2.0 ** -30: 0x3F81,  # just above the midpoint: a float detour would tie down
+        -(1.0 + 2.0 ** -8 + 2.0 ** -30): 0xBF81,
+    }
+    for v, bits in cases.items():
+        assert int(oracle.bf16_from_double([v])[0]) == bits, v
+
+
+def test_bf16_is_nearest_of_neighbours():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal(50000) * 3.0
+    b = oracle.bf16_from_double(v)
+    r = oracle.bf16_to_double(b)
+    up = oracle.bf16_to_double((b.astype(np.int32) + 1).astype(np.uint16))
+    dn = oracle.bf16_to_double((b.astype(np.int32) - 1).astype(np.uint16))
+    assert np.all(np.abs(v - r) <= np.abs(v - up))
+    assert np.all(np.abs(v - r) <= np.abs(v - dn))
+
+
+# ------------------------------------------------------------------------------------ e4m3
+def test_e4m3_decode_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert set(np.nonzero(nan)[0]) == {0x7F, 0xFF}
+    np.testing.assert_array_equal(np.isnan(ours), nan)
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_round_to_nearest_even():
+    vals = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # finite positive grid
+    mids = (vals[:-1] + vals[1:]) / 2
+    probes = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                             np.nextafter(mids.astype(np.float32), np.float32(1e9))]).astype(np.float32)
+    rng = np.random.default_rng(3)
+    probes = np.concatenate([probes, (rng.standard_normal(20000) * 50).astype(np.float32)])
+    probes = np.concatenate([probes, -probes])
+    probes = probes[np.abs(probes) < 464.0]  # torch turns larger magnitudes into NaN; we saturate
+    ours = oracle.e4m3_encode(probes)
+    ref = torch.from_numpy(probes).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_e4m3_saturates():
+    c = oracle.e4m3_encode(np.array([464.0, 500.0, 1e30, -1e30], np.float32))
+    np.testing.assert_array_equal(c, [0x7E, 0x7E, 0x7E, 0xFE])
+
+
+def test_quant_1x128_error_bound_and_zero_block():
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal((7, 384)) * np.exp(rng.standard_normal((7, 1)) * 3)
+    v[3, 128:256] = 0.0
+    q, s = oracle.quant_1x128(v)
+    assert s[3, 1] == 1.0 and np.all(q[3, 128:256] == 0)
+    deq = oracle.e4m3_decode(q) * np.repeat(s, 128, axis=1)
+    bound = np.maximum(np.abs(v) * 2.0 ** -4, np.repeat(s, 128, axis=1) * 2.0 ** -10)
+    assert np.all(np.abs(v - deq) <= bound * (1 + 1e-6))
+    # the block maximum lands on the largest code
+    for r in range(7):
+        for b in range(3):
+            if r == 3 and b == 1:
+                continue
+            blk = v[r, b * 128:(b + 1) * 128]
+            i = int(np.argmax(np.abs(blk)))
+            assert (q[r, b * 128 + i] & 0x7F) == 0x7E
+            assert s[r, b] == np.float32(np.abs(blk).max() / 448.0)
+
+
+def test_quant_weight_128x128_matches_row_rule():
+    rng = np.random.default_rng(5)
+    w = oracle.bf16_from_double(rng.standard_normal((256, 384)) * 0.02)
+    q, s = oracle.quant_weight_128x128(w)
+    wd = oracle.bf16_to_double(w)
+    for br in range(2):
+        for bc in range(3):
+            blk = wd[br * 128:(br + 1) * 128, bc * 128:(bc + 1) * 128]
+            sc = np.float32(np.abs(blk).max() / 448.0)
+            assert s[br, bc] == sc
+            ref = torch.from_numpy((blk / np.float64(sc)).astype(np.float32)).to(torch.float8_e4m3fn)
+            np.testing.assert_array_equal(q[br * 128:(br + 1) * 128, bc * 128:(bc + 1) * 128],
+                                          ref.view(torch.uint8).numpy())
+
+
+# ------------------------------------------------------------------------------------ logits
+def test_router_logits_match_torch_fp64_matmul():
+    rng = np.random.default_rng(6)
+    x = oracle.bf16_from_double(rng.standard_normal((33, 200)))
+    w = (rng.standard_normal((12, 200)) * 0.02).astype(np.float32)
+    ours = oracle.router_logits(x, w)
+    ref = (torch.from_numpy(oracle.bf16_to_double(x)) @ torch.from_numpy(w.astype(np.float64)).T).numpy()
+    np.testing.assert_allclose(ours, ref.astype(np.float32), rtol=1e-6, atol=1e-7)
+
+
+# ------------------------------------------------------------------------------------ routing
+def _brute_topk(key, allowed, k):
+    """k-subset of the allowed entries with the largest key sum, sorted by key descending"""
+    best, best_sum = None, -math.inf
+    for sub in itertools.combinations([i for i in range(len(key)) if allowed[i]], k):
+        s = sum(float(key[i]) for i in sub)
+        if s > best_sum:
+            best, best_sum = sub, s
+    return sorted(best, key=lambda i: (-float(key[i]), i))
+
+
+def test_softmax_topk_brute_force_and_torch_weights():
+    rng = np.random.default_rng(7)
+    T, E, k = 200, 8, 2
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    for renorm in (False, True):
+        idx, w = oracle.route(logits, None, k, score=oracle.SOFTMAX, renorm=renorm)
+        p = torch.softmax(torch.from_numpy(logits.astype(np.float64)), dim=-1).numpy()
+        for t in range(T):
+            assert list(idx[t]) == _brute_topk(logits[t], [1] * E, k)
+            ref = p[t, idx[t]]
+            if renorm:
+                ref = ref / ref.sum()
+            np.testing.assert_allclose(w[t], ref, rtol=1e-6)
+        tv, ti = torch.from_numpy(logits).topk(k, dim=-1)
+        np.testing.assert_array_equal(idx, ti.numpy())
+
+
+def _sigmoid_f32(l):
+    return (1.0 / (1.0 + np.exp(-l.astype(np.float64)))).astype(np.float32)
+
+
+def test_grouped_sigmoid_topk_brute_force():
+    rng = np.random.default_rng(8)
+    T, E, G, Gk, k = 60, 16, 8, 4, 3
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    idx, w = oracle.route(logits, bias, k, G, Gk, oracle.SIGMOID, True, 2.5)
+    gs = E // G
+    for t in range(T):
+        s = _sigmoid_f32(logits[t])
+        key = s + bias
+        gscore = [float(np.sort(key[g * gs:(g + 1) * gs])[-2:].astype(np.float32).sum(dtype=np.float32))
+                  for g in range(G)]
+        best_groups, best = None, -math.inf
+        for sub in itertools.combinations(range(G), Gk):
+            tot = sum(gscore[g] for g in sub)
+            if tot > best:
+                best_groups, best = sub, tot
+        allowed = [1 if (e // gs) in best_groups else 0 for e in range(E)]
+        sel = _brute_topk(key, allowed, k)
+        assert list(idx[t]) == sel
+        ref = s[sel].astype(np.float64)
+        np.testing.assert_allclose(w[t], ref / ref.sum() * 2.5, rtol=1e-6)
+        assert abs(float(w[t].sum()) - 2.5) < 1e-5
+
+
+def test_group_score_is_top2_sum_not_max():
+    E, G = 8, 4  # groups of two experts
+    logits = np.full((1, E), -10.0, np.float32)
+    logits[0, 0] = 3.0  # group 0: one strong expert, one weak -> max wins, top-2 sum loses
+    logits[0, 2] = logits[0, 3] = 1.0  # group 1: two good experts
+    idx, _ = oracle.route(logits, None, 2, G, 1, oracle.SIGMOID, True, 1.0)
+    assert sorted(idx[0]) == [2, 3]
+
+
+def test_bias_selects_but_does_not_weigh():
+    E = 4
+    logits = np.array([[0.5, 0.4, 0.0, -1.0]], np.float32)
+    bias = np.array([0.0, 0.0, 0.5, 0.0], np.float32)
+    idx, w = oracle.route(logits, bias, 2, 1, 1, oracle.SIGMOID, False, 1.0)
+    assert list(idx[0]) == [2, 0]  # s+bias: 0.5+0.5 beats sigmoid(0.5)
+    np.testing.assert_allclose(w[0], _sigmoid_f32(logits[0])[[2, 0]], rtol=1e-7)
+
+
+def test_ties_break_to_lower_index():
+    logits = np.zeros((3, 256), np.float32)
+    idx, _ = oracle.route(logits, None, 8, 8, 4, oracle.SIGMOID, True, 2.5)
+    np.testing.assert_array_equal(idx, np.tile(np.arange(8), (3, 1)))
+    idx, _ = oracle.route(logits[:, :8], None, 2, score=oracle.SOFTMAX)
+    np.testing.assert_array_equal(idx, np.tile(np.arange(2), (3, 1)))
+    # a tie among groups only: groups 1..3 tie, group 0 is worse -> groups 1, 2 kept
+    l = np.zeros((1, 16), np.float32)
+    l[0, 0:4] = -1.0
+    idx, _ = oracle.route(l, None, 8, 4, 2, oracle.SIGMOID, True, 1.0)
+    assert sorted(idx[0]) == list(range(4, 12))
+
+
+def test_p3_worked_example_histogram():
+    """The page's seeded routing snippet: recomputed logits routed by the oracle give the printed
+    per-expert and per-GPU counts."""
+    g = json.load(open(os.path.join(GOLDEN, "p3_routing_histogram.json")))
+    torch.manual_seed(g["seed"])
+    tokens = torch.randn(g["tokens"], g["hidden"])
+    lin = torch.nn.Linear(g["hidden"], g["experts"])
+    with torch.no_grad():
+        logits = lin(tokens).numpy()
+    idx, _ = oracle.route(logits, None, g["top_k"], score=oracle.SOFTMAX)
+    counts, offsets, _, _ = oracle.permute(idx, g["experts"])
+    assert counts.min() == g["expert_count_min"] and counts.max() == g["expert_count_max"]
+    assert counts.sum() == g["assignments"] == offsets[-1]
+    per_gpu = counts.reshape(g["gpus"], -1).sum(axis=1)
+    assert per_gpu.min() == g["gpu_count_min"] and per_gpu.max() == g["gpu_count_max"]
+    _, ti = torch.from_numpy(logits).topk(g["top_k"], dim=-1)
+    np.testing.assert_array_equal(idx, ti.numpy())
+
+
+# ------------------------------------------------------------------------------------ permute
+def test_permute_invariants_and_stable_sort():
+    rng = np.random.default_rng(9)
+    T, E, k = 500, 16, 4
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, inv_pos, row_token = oracle.permute(idx, E)
+    np.testing.assert_array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert offsets[0] == 0 and offsets[-1] == T * k
+    np.testing.assert_array_equal(np.diff(offsets), counts)
+    # bijection: every row used once, and it holds the right token
+    assert sorted(inv_pos.ravel().tolist()) == list(range(T * k))
+    np.testing.assert_array_equal(row_token[inv_pos], np.repeat(np.arange(T), k).reshape(T, k))
+    # expert-major, ascending token: the stable sort of the flattened (token, slot) list by expert
+    order = np.argsort(idx.ravel(), kind="stable")
+    np.testing.assert_array_equal(row_token, order // k)
+
+
+def test_gather_rows_matches_fancy_indexing():
+    rng = np.random.default_rng(10)
+    x = rng.integers(0, 65535, (40, 24), dtype=np.uint16)
+    rt = rng.integers(0, 40, 100).astype(np.int32)
+    np.testing.assert_array_equal(oracle.gather_rows(x, rt), x[rt])
+
+
+# ------------------------------------------------------------------------------------ experts
+def _torch_swiglu(x_bf16, w_gu, w_d, I):
+    x = torch.from_numpy(oracle.bf16_to_double(x_bf16))
+    gu = torch.from_numpy(oracle.bf16_to_double(w_gu))
+    d = torch.from_numpy(oracle.bf16_to_double(w_d))
+    g = x @ gu[:I].T
+    u = x @ gu[I:].T
+    a = (torch.nn.functional.silu(g) * u).to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    return (a @ d.T).numpy()
+
+
+def test_expert_ffn_bf16_matches_torch_swiglu():
+    rng = np.random.default_rng(11)
+    m, h, I = 9, 256, 128
+    x = oracle.bf16_from_double(rng.standard_normal((m, h)))
+    w_gu = oracle.bf16_from_double(rng.standard_normal((2 * I, h)) * 0.02)
+    w_d = oracle.bf16_from_double(rng.standard_normal((h, I)) * 0.02)
+    ours = oracle.expert_ffn_bf16(x, w_gu, w_d)
+    ref = _torch_swiglu(x, w_gu, w_d, I)
+    assert np.abs(ours - ref).max() <= 1e-3 * np.abs(ref).max()
+    # swapping gate and up is a different function: the pin must be able to see it
+    swapped = np.concatenate([w_gu[I:], w_gu[:I]])
+    assert np.abs(_torch_swiglu(x, swapped, w_d, I) - ours).max() > 1e-2 * np.abs(ref).max()
+
+
+def test_expert_ffn_fp8_matches_torch_dequantised():
+    rng = np.random.default_rng(12)
+    m, h, I = 5, 256, 256
+    x = oracle.bf16_from_double(rng.standard_normal((m, h)))
+    w_gu = oracle.bf16_from_double(rng.standard_normal((2 * I, h)) * 0.02)
+    w_d = oracle.bf16_from_double(rng.standard_normal((h, I)) * 0.02)
+    xq, xs = oracle.quant_1x128(oracle.bf16_to_double(x))
+    gq, gs = oracle.quant_weight_128x128(w_gu)
+    dq, ds = oracle.quant_weight_128x128(w_d)
+    ours = oracle.expert_ffn_fp8(xq, xs, gq, gs, dq, ds)
+
+    def deq(q, s, bm, bn):
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64)
+        return v * torch.from_numpy(s.astype(np.float64)).repeat_interleave(bm, 0).repeat_interleave(bn, 1)
+
+    xdq = deq(xq, xs, 1, 128)
+    g = xdq @ deq(gq, gs, 128, 128)[:I].T
+    u = xdq @ deq(gq, gs, 128, 128)[I:].T
+    a = (torch.nn.functional.silu(g) * u).numpy()
+    aq, as_ = oracle.quant_1x128(a)
+    ref = (deq(aq, as_, 1, 128) @ deq(dq, ds, 128, 128).T).numpy()
+    assert np.abs(ours - ref).max() <= 1e-4 * np.abs(ref).max()
+
+
+# ------------------------------------------------------------------------------------ combine
+def test_combine_identity_experts_closed_form():
+    """Identity experts: y = x * sum_j w_j (+ x with an identity shared expert)."""
+    rng = np.random.default_rng(13)
+    T, k, h = 50, 8, 64
+    x = oracle.bf16_from_double(rng.standard_normal((T, h)))
+    xd = oracle.bf16_to_double(x)
+    w = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    o = np.repeat(xd[:, None, :], k, axis=1)
+    y = oracle.combine(o, w, None)
+    ref = oracle.bf16_from_double(xd * w.astype(np.float64).sum(axis=1, keepdims=True))
+    np.testing.assert_array_equal(y, ref)
+    y2 = oracle.combine(o, w, xd)
+    ref2 = oracle.bf16_from_double(xd * (w.astype(np.float64).sum(axis=1, keepdims=True) + 1.0))
+    np.testing.assert_array_equal(y2, ref2)
+    # renormalised softmax weights sum to one: identity experts return x itself
+    _, wr = oracle.route(rng.standard_normal((T, 8)).astype(np.float32), None, 2, score=oracle.SOFTMAX, renorm=True)
+    np.testing.assert_array_equal(oracle.combine(o[:, :2], wr, None), x)
+
+
+def test_forward_single_expert_is_dense_mlp():
+    """E = 1, k = 1, softmax: every token goes to expert 0 with weight 1 -> a dense SwiGLU MLP."""
+    rng = np.random.default_rng(14)
+    T, h, I = 20, 128, 128
+    x = oracle.bf16_from_double(rng.standard_normal((T, h)))
+    w_r = (rng.standard_normal((1, h)) * 0.02).astype(np.float32)
+    w_gu = oracle.bf16_from_double(rng.standard_normal((2 * I, h)) * 0.02)
+    w_d = oracle.bf16_from_double(rng.standard_normal((h, I)) * 0.02)
+    out = oracle.forward(x, w_r, None, [(w_gu, w_d)], None, k=1, renorm=False)
+    np.testing.assert_array_equal(out["topk_idx"], 0)
+    np.testing.assert_allclose(out["topk_w"], 1.0)
+    ref = _torch_swiglu(x, w_gu, w_d, I)
+    y = oracle.bf16_to_double(out["y"])
+    assert np.abs(y - ref).max() <= 2 ** -8 * np.abs(ref).max()
+
+
+# ------------------------------------------------------------------------------------ imbalance
+def _p5_sampler(n_experts, top_k, n_tokens, skew, seed):
+    """Token-to-expert counts under a shuffled power-law popularity, drawn in the same order as the
+    page's simulation so the printed numbers reproduce."""
+    rng = random.Random(seed)
+    popularity = [(r + 1) ** (-skew) for r in range(n_experts)]
+    rng.shuffle(popularity)
+    experts = list(range(n_experts))
+    counts = [0] * n_experts
+    for _ in range(n_tokens):
+        picked = set()
+        while len(picked) < top_k:
+            picked.add(rng.choices(experts, weights=popularity)[0])
+        for e in picked:
+            counts[e] += 1
+    return counts
+
+
+def test_p5_imbalance_table():
+    g = json.load(open(os.path.join(GOLDEN, "p5_imbalance.json")))
+    c = _p5_sampler(g["experts"], g["top_k"], g["tokens"], g["skew"], g["seed"])
+    assert max(c) == g["hottest"] and min(c) == g["coldest"]
+    assert sum(c) / len(c) == g["average"]
+    for ep, val in g["contiguous_imbalance"].items():
+        assert round(oracle.imbalance(c, int(ep)), 2) == pytest.approx(val)
