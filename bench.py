@@ -1,0 +1,415 @@
+"""MoE-layer tokens/s on one GB300 (or N independent replicas), with roofline and CPU-oracle baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl {ours,reference}]
+
+One step = one pass of the whole layer (router GEMM, top-k, dispatch, gate/up and down grouped
+GEMMs, combine) over one batch of synthetic tokens, through the C ABI (moe_forward). The default
+workload is the DeepSeek-V3-shaped prefill layer (16384 tokens, h 7168, 256 routed experts top-8 +
+1 shared, intermediate 2048); its 22.6 GB of expert weights are read every step, far more than L2.
+
+Prints ONE JSON line on rank 0. ``--impl reference`` times the CPU oracle instead (on the host cores,
+bounded samples of the same workload, nothing on the GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/sec on 1 GB300; % of roofline (HBM or tensor-pipe)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def layer_counts(wl, active_experts):
+    """Algorithmic FLOPs and bytes of one layer step (inputs, outputs and the weights that must be
+    read; the permute buffers are overhead, not algorithmic)."""
+    T, h, E, k, I, Is = wl.T, wl.h, wl.E, wl.k, wl.I, wl.I_shared
+    wbytes = 1 if wl.dtype == "fp8" else 2
+    gemm_flops = 6.0 * T * k * h * I + 6.0 * T * h * Is
+    flops = 2.0 * T * h * E + gemm_flops
+    bytes_ = (2.0 * T * h * 2  # x in, y out (bf16)
+              + 4.0 * E * h + (4.0 * E if wl.bias_range is not None else 0.0)  # router weight, bias
+              + active_experts * 3.0 * h * I * wbytes + 3.0 * h * Is * wbytes)
+    return flops, gemm_flops, bytes_
+
+
+def gemm_traffic_from_profile(wl):
+    """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it was taken on the
+    current kernel source and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "routing_dispatch_expert_gb300", "csrc", "gemm.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if d.get("kernel_source_sha256") != sha or d.get("workload") != wl.name:
+        return None
+    return d.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background during a timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = [l.split(", ") for l in open(self.path).read().strip().splitlines() if l.count(",") >= 8]
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        # samples under load: the top half of the observed power draw
+        load = sm
+        if power and len(power) == len(sm):
+            thr = float(np.median(power))
+            load = [s for s, p in zip(sm, power) if p >= thr] or sm
+        return {"sm_mhz": float(np.median(load)) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def time_cpu_oracle(wl, budget_s):
+    """The oracle as it stands, on a bounded sample of the workload's tokens, on the host cores.
+
+    Sample: S tokens of the workload go through the oracle's router GEMM, top-k, permutation,
+    dispatch copy, expert FFNs of all their S*k routed rows (plus S shared-expert rows) and combine.
+    So that one expert's weights suffice on the host, every routed row is evaluated with routed
+    expert 0's weights (the same shapes, so the same arithmetic cost). Returns (tokens/s, S, seconds).
+    """
+    import oracle
+    import synth
+
+    kw = dict(k=wl.k, n_group=wl.n_group, topk_group=wl.topk_group,
+              score=oracle.SOFTMAX if wl.score == "softmax" else oracle.SIGMOID, renorm=wl.renorm,
+              routed_scale=wl.routed_scale)
+    w_r = synth.router_weight(wl)
+    bias = synth.bias(wl)
+    mu = synth.skew_shift(wl, w_r)
+    gu0, d0 = synth.expert_weights(wl, 0)
+    sh = synth.expert_weights(wl, "shared") if wl.has_shared else None
+
+    def run(S):
+        x = synth.activations(wl, mu, 0, S)
+        t0 = time.perf_counter()
+        logits = oracle.router_logits(x, w_r)
+        idx, w = oracle.route(logits, bias, **kw)
+        _, _, inv_pos, row_token = oracle.permute(idx, wl.E)
+        xd = oracle.gather_rows(x, row_token)
+        if wl.dtype == "fp8":
+            xq, xs = oracle.quant_1x128(oracle.bf16_to_double(xd))
+            (gq, gs), (dq, ds) = oracle.quant_weight_128x128(gu0), oracle.quant_weight_128x128(d0)
+            o_rows = oracle.expert_ffn_fp8(xq, xs, gq, gs, dq, ds)
+            shared = None
+            if sh is not None:
+                sq, ss = oracle.quant_1x128(oracle.bf16_to_double(x))
+                (a, b), (c, d) = oracle.quant_weight_128x128(sh[0]), oracle.quant_weight_128x128(sh[1])
+                shared = oracle.expert_ffn_fp8(sq, ss, a, b, c, d)
+        else:
+            o_rows = oracle.expert_ffn_bf16(xd, gu0, d0)
+            shared = oracle.expert_ffn_bf16(x, sh[0], sh[1]) if sh is not None else None
+        oracle.combine(o_rows[inv_pos.reshape(-1)].reshape(S, wl.k, wl.h), w, shared)
+        return time.perf_counter() - t0
+
+    S = 2
+    dt = run(S)
+    S = int(max(1, min(wl.T, S * budget_s / max(dt, 1e-6))))
+    dt = run(S)
+    return S / dt, S, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v and v.isdigit() else host_cores()
+
+
+def reference_arm(args, wl, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    budget = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_cpu_oracle(wl, budget)
+    vals, samples, secs = [], [], []
+    for _ in range(args.steps):
+        v, S, dt = time_cpu_oracle(wl, budget)
+        vals.append(v)
+        samples.append(S)
+        secs.append(dt)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": float(np.median(secs)) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": omp_threads(), "kind": "oracle",
+                         "sample": f"per step {int(np.median(samples))} of the workload's tokens through the whole "
+                                   "oracle layer (routed rows evaluated with one expert's weights, same shapes)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, world):
+    return {"workload": wl.name, "T": wl.T, "h": wl.h, "E": wl.E, "k": wl.k, "I": wl.I, "I_shared": wl.I_shared,
+            "n_group": wl.n_group, "topk_group": wl.topk_group, "score": wl.score, "expert_dtype": wl.dtype,
+            "zipf_s": wl.zipf_s, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: every step reads all active expert weights (GBs) once"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="dsv3_prefill")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, wl, rank, world)
+        return
+
+    import torch
+
+    import routing_dispatch_expert_gb300 as rde
+    from routing_dispatch_expert_gb300 import build as pkg_build
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0 or world > 1:
+        pkg_build.build()
+        synth.build()
+    if dist is not None:
+        dist.barrier()
+    rde.load()
+
+    dev = torch.device("cuda", local_rank)
+    cfg = rde.make_config(T=wl.T, h=wl.h, E=wl.E, k=wl.k, I=wl.I, I_shared=wl.I_shared, n_group=wl.n_group,
+                          topk_group=wl.topk_group, score=wl.score, renorm=wl.renorm, routed_scale=wl.routed_scale,
+                          dtype=wl.dtype)
+    inp = synth.device_inputs(wl, torch, device=dev)
+    wts = dict(w_gu=inp["w_gu"], w_d=inp["w_d"], w_gu_shared=inp["w_gu_shared"], w_d_shared=inp["w_d_shared"])
+    if wl.dtype == "fp8":
+        wts["w_gu"], wts["s_gu"] = rde.quantize_weights_fp8(inp["w_gu"])
+        wts["w_d"], wts["s_d"] = rde.quantize_weights_fp8(inp["w_d"])
+        if wl.has_shared:
+            wts["w_gu_shared"], wts["s_gu_shared"] = rde.quantize_weights_fp8(inp["w_gu_shared"])
+            wts["w_d_shared"], wts["s_d_shared"] = rde.quantize_weights_fp8(inp["w_d_shared"])
+        del inp["w_gu"], inp["w_d"]
+    weights = rde.Weights(w_router=inp["w_router"], bias=inp["bias"], **wts)
+    ws = rde.alloc_workspace(cfg, dev)
+    rde.device_status(cfg, ws)
+    x = inp["x"]
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    # warm-up (untimed)
+    for _ in range(args.warmup):
+        rde.forward(cfg, x, weights, y, ws)
+    torch.cuda.synchronize(dev)
+    status = rde.device_status(cfg, ws)
+    if status != 0:
+        raise SystemExit(f"device status {status} after warm-up")
+    counts = rde.ws_view(ws, cfg, "counts", torch.int32, (wl.E,)).cpu().numpy()
+    active = int((counts > 0).sum())
+
+    # timed region: K whole-layer steps; the grouped-GEMM pair (moe_expert_ffn) is timed separately
+    # on the same stream by running the steps through their own entry points
+    lay = rde.workspace_layout(cfg)
+    R = wl.T * wl.k
+    R_tot = R + (wl.T if wl.has_shared else 0)
+    v = lambda name, dt, shape: rde.ws_view(ws, cfg, name, dt, shape)  # noqa: E731
+    xd_dt = torch.uint8 if wl.dtype == "fp8" else torch.bfloat16
+    it = dict(logits=v("logits", torch.float32, (wl.T, wl.E)), idx=v("topk_idx", torch.int32, (wl.T, wl.k)),
+              w=v("topk_w", torch.float32, (wl.T, wl.k)), counts=v("counts", torch.int32, (wl.E,)),
+              offsets=v("offsets", torch.int32, (wl.E + 1,)), inv_pos=v("inv_pos", torch.int32, (wl.T, wl.k)),
+              row_token=v("row_token", torch.int32, (R,)), row_weight=v("row_weight", torch.float32, (R,)),
+              xd=v("xd", xd_dt, (R_tot, wl.h)), yd=v("yd", torch.bfloat16, (R_tot, wl.h)))
+    xs = v("xd_scales", torch.float32, (R_tot, wl.h // 128)) if wl.dtype == "fp8" else None
+
+    def step_split(ev_a, ev_b):
+        rde.route(cfg, x, weights, it["idx"], it["w"], logits=it["logits"], ws=ws)
+        rde.dispatch(cfg, x, it["idx"], it["w"], it["counts"], it["offsets"], it["inv_pos"], it["row_token"],
+                     it["row_weight"], it["xd"], xs, ws)
+        ev_a.record(stream)
+        rde.expert_ffn(cfg, weights, it["xd"], xs, it["offsets"], it["row_weight"], it["yd"], ws)
+        ev_b.record(stream)
+        rde.combine(cfg, it["yd"], it["inv_pos"], y)
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] if world == 1 else local_rank
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        step_split(*evs[0])
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index) as clk:
+        n0 = rde.launch_count()
+        start.record(stream)
+        for i in range(args.steps):
+            step_split(*evs[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        n1 = rde.launch_count()
+        if dist is not None:
+            dist.barrier()
+    clocks = clk.summary()
+    ms_total = start.elapsed_time(end)
+    gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    # moe_forward as one call (the fused entry point) for the headline
+    fstart, fend = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    fstart.record(stream)
+    for _ in range(args.steps):
+        rde.forward(cfg, x, weights, y, ws)
+    fend.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_fwd = fstart.elapsed_time(fend) / args.steps
+    ms_step = ms_total / args.steps
+
+    # end to end through the public API with host buffers: pinned x in, y out, every step
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    torch.cuda.synchronize(dev)
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        rde.forward(cfg, x_dev, weights, y, ws)
+        y_host.copy_(y, non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e_s.elapsed_time(e_e) / e2e_steps
+
+    # max over ranks
+    vals = torch.tensor([ms_step, ms_e2e, gemm_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms_step, ms_e2e, gemm_ms = vals.tolist()
+    status = rde.device_status(cfg, ws)
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+
+    peaks, peaks_kind = load_peaks()
+    flops, gemm_flops, bytes_ = layer_counts(wl, active)
+    p_tc = peaks["bf16_tflops"] * 1e12
+    p_hbm = peaks["hbm_gbs"] * 1e9
+    t_roof = max(flops / p_tc, bytes_ / p_hbm)
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    traffic = gemm_traffic_from_profile(wl)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, S, dt = time_cpu_oracle(wl, 12.0)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": omp_threads(), "kind": "oracle",
+               "sample": f"{S} of the workload's tokens through the whole oracle layer in {dt:.1f} s "
+                         "(routed rows evaluated with one expert's weights, same shapes)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * wl.T / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl, world),
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": gemm_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                         "kernel": "grouped_gemm_bf16_kernel (gate/up + down launches of one step)",
+                         "peak_kind": f"bf16 burst, {peaks_kind}",
+                         "frac_of_sustained": gemm_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])},
+            "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3), "flops": flops,
+                               "bytes": bytes_, "active_experts": active,
+                               "bound": "tensor" if flops / p_tc >= bytes_ / p_hbm else "hbm",
+                               "peaks": peaks_kind},
+            "ms_moe_forward": ms_fwd, "ms_expert_ffn": gemm_ms,
+            "e2e": {"value": world * wl.T / (ms_e2e * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                    "d2h_bytes_per_step": int(y.numel() * y.element_size())},
+            "gpu_launches": int(n1 - n0),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

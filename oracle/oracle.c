@@ -333,9 +333,9 @@ static double orc_silu(double g) { return g / (1.0 + exp(-g)); }
 
 ORC_API void orc_expert_ffn_bf16(const uint16_t* x, int64_t m, int64_t h, int64_t I, const uint16_t* w_gu,
                                  const uint16_t* w_d, double* out) {
-#pragma omp parallel for schedule(dynamic, 1)
+  double* a = (double*)malloc(sizeof(double) * I);
   for (int64_t r = 0; r < m; ++r) {
-    double* a = (double*)malloc(sizeof(double) * I);
+#pragma omp parallel for schedule(static)
     for (int64_t c = 0; c < I; ++c) {
       double g = 0.0, u = 0.0;
       for (int64_t d = 0; d < h; ++d) {
@@ -345,13 +345,14 @@ ORC_API void orc_expert_ffn_bf16(const uint16_t* x, int64_t m, int64_t h, int64_
       }
       a[c] = orc_bf16_to_double(orc_bf16_from_double(orc_silu(g) * u));
     }
+#pragma omp parallel for schedule(static)
     for (int64_t d = 0; d < h; ++d) {
       double o = 0.0;
       for (int64_t c = 0; c < I; ++c) o += a[c] * orc_bf16_to_double(w_d[d * I + c]);
       out[r * h + d] = o;
     }
-    free(a);
   }
+  free(a);
 }
 
 /* FP8 block-scaled variant ([PPLX] "Quantization"): operands are e4m3 codes with fp32
@@ -363,11 +364,11 @@ ORC_API void orc_expert_ffn_fp8(const uint8_t* xq, const float* xs, int64_t m, i
                                 const uint8_t* w_gu_q, const float* w_gu_s, const uint8_t* w_d_q,
                                 const float* w_d_s, double* out) {
   int64_t hb = h / 128, ib = I / 128;
-#pragma omp parallel for schedule(dynamic, 1)
+  double* a = (double*)malloc(sizeof(double) * I);
+  uint8_t* aq = (uint8_t*)malloc(I);
+  float* as = (float*)malloc(sizeof(float) * ib);
   for (int64_t r = 0; r < m; ++r) {
-    double* a = (double*)malloc(sizeof(double) * I);
-    uint8_t* aq = (uint8_t*)malloc(I);
-    float* as = (float*)malloc(sizeof(float) * ib);
+#pragma omp parallel for schedule(static)
     for (int64_t c = 0; c < I; ++c) {
       double g = 0.0, u = 0.0;
       for (int64_t d = 0; d < h; ++d) {
@@ -378,6 +379,7 @@ ORC_API void orc_expert_ffn_fp8(const uint8_t* xq, const float* xs, int64_t m, i
       a[c] = orc_silu(g) * u;
     }
     orc_quant_1x128(a, 1, I, aq, as);
+#pragma omp parallel for schedule(static)
     for (int64_t d = 0; d < h; ++d) {
       double o = 0.0;
       for (int64_t c = 0; c < I; ++c)
@@ -385,10 +387,10 @@ ORC_API void orc_expert_ffn_fp8(const uint8_t* xq, const float* xs, int64_t m, i
              (double)w_d_s[(d / 128) * ib + c / 128];
       out[r * h + d] = o;
     }
-    free(a);
-    free(aq);
-    free(as);
   }
+  free(a);
+  free(aq);
+  free(as);
 }
 
 /* ------------------------------------------------------------------------------------------

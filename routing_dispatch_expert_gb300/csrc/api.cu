@@ -1,0 +1,397 @@
+// C ABI of the library: argument checks, workspace layout and the launch sequence of each step.
+// Declarations and the contract of every entry point are in include/moe.h.
+#include <stdio.h>
+
+#include <atomic>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+#define MOE_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_launches{0};
+
+void counted(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return MOE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int check_config(const moe_config* c) {
+  if (!c) return fail(MOE_ERR_INVALID, "cfg is NULL");
+  if (c->T < 0 || c->h <= 0 || c->E <= 0 || c->k <= 0 || c->I <= 0 || c->I_shared < 0)
+    return fail(MOE_ERR_INVALID, "T must be >= 0 and h, E, k, I positive, I_shared >= 0");
+  if (c->k > c->E || c->k > 32) return fail(MOE_ERR_INVALID, "k must lie in [1, min(E, 32)]");
+  if (c->n_group < 1 || c->n_group > 32 || c->E % c->n_group != 0)
+    return fail(MOE_ERR_INVALID, "n_group must lie in [1, 32] and divide E");
+  if (c->topk_group < 1 || c->topk_group > c->n_group)
+    return fail(MOE_ERR_INVALID, "topk_group must lie in [1, n_group]");
+  if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k)
+    return fail(MOE_ERR_INVALID, "the kept groups hold fewer than k experts");
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return fail(MOE_ERR_INVALID, "unknown score");
+  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_BLOCK128) return fail(MOE_ERR_INVALID, "unknown dtype");
+  if (c->E > 1024) return fail(MOE_ERR_UNSUPPORTED, "E > 1024");
+  if (c->h % 256 != 0) return fail(MOE_ERR_UNSUPPORTED, "h must be a multiple of 256");
+  if (c->I % 128 != 0) return fail(MOE_ERR_UNSUPPORTED, "I must be a multiple of 128");
+  if (c->I_shared != 0 && c->I_shared != c->I) return fail(MOE_ERR_UNSUPPORTED, "I_shared must be 0 or I");
+  if ((int64_t)c->T * (c->k + 1) > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "T * (k + 1) exceeds int32 rows");
+  return MOE_OK;
+}
+
+struct Layout {
+  moe_ws_layout l;
+  int64_t R, R_tot;
+};
+
+Layout make_layout(const moe_config* c) {
+  Layout L;
+  const int64_t T = c->T, E = c->E, k = c->k, h = c->h, I = c->I;
+  const bool fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
+  L.R = T * k;
+  L.R_tot = L.R + (c->I_shared > 0 ? T : 0);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  moe_ws_layout& l = L.l;
+  l.logits = take(sizeof(float) * T * E);
+  l.topk_idx = take(sizeof(int32_t) * T * k);
+  l.topk_w = take(sizeof(float) * T * k);
+  l.counts = take(sizeof(int32_t) * E);
+  l.offsets = take(sizeof(int32_t) * (E + 1));
+  l.inv_pos = take(sizeof(int32_t) * T * k);
+  l.row_token = take(sizeof(int32_t) * L.R);
+  l.row_weight = take(sizeof(float) * L.R);
+  l.xd = take((fp8 ? 1 : 2) * L.R_tot * h);
+  l.xd_scales = take(fp8 ? sizeof(float) * L.R_tot * (h / 128) : 0);
+  l.hbuf = take((fp8 ? 1 : 2) * L.R_tot * I);
+  l.h_scales = take(fp8 ? sizeof(float) * L.R_tot * (I / 128) : 0);
+  l.yd = take(2 * L.R_tot * h);
+  l.scratch = take(256 + sizeof(int32_t) * moe::dispatch_scratch_ints(c->T, c->E));
+  l.total = o;
+  return L;
+}
+
+int* status_ptr(void* ws, const moe_ws_layout& l) {
+  return reinterpret_cast<int*>(static_cast<char*>(ws) + l.scratch);
+}
+int32_t* hist_ptr(void* ws, const moe_ws_layout& l) {
+  return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + l.scratch + 256);
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int check_ws(void* ws, size_t ws_bytes, const Layout& L) {
+  if (!ws) return fail(MOE_ERR_INVALID, "ws is NULL");
+  if (!aligned16(ws)) return fail(MOE_ERR_INVALID, "ws must be 16-byte aligned");
+  if (ws_bytes < L.l.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace too small: " + std::to_string(ws_bytes) + " < " +
+                                       std::to_string(L.l.total) + " bytes");
+  return MOE_OK;
+}
+
+#define REQUIRE_PTR(p, name)                                                   \
+  do {                                                                         \
+    if (!(p)) return fail(MOE_ERR_INVALID, std::string(name) + " is NULL");    \
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID, std::string(name) + " must be 16-byte aligned"); \
+  } while (0)
+
+int do_route(const moe_config* c, const void* x, const moe_weights* w, float* logits, int flags, int32_t* topk_idx,
+             float* topk_w, cudaStream_t stream) {
+  cudaError_t e;
+  if (!(flags & MOE_LOGITS_GIVEN)) {
+    e = moe::launch_router_gemm(x, w->w_router, logits, c->T, c->h, c->E, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
+    if (c->T > 0) counted(1);
+  }
+  moe::TopkDesc d;
+  d.logits = logits;
+  d.bias = w ? w->bias : nullptr;
+  d.topk_idx = topk_idx;
+  d.topk_w = topk_w;
+  d.T = c->T;
+  d.E = c->E;
+  d.k = c->k;
+  d.n_group = c->n_group;
+  d.topk_group = c->topk_group;
+  d.score = c->score;
+  d.renorm = c->renormalize;
+  d.routed_scale = c->routed_scale;
+  if (c->score == MOE_SCORE_SOFTMAX) d.bias = nullptr;
+  e = moe::launch_topk(d, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  if (c->T > 0) counted(1);
+  return MOE_OK;
+}
+
+int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, const float* topk_w, int32_t* counts,
+                int32_t* offsets, int32_t* inv_pos, int32_t* row_token, float* row_weight, void* xd, float* xd_scales,
+                void* ws, const Layout& L, cudaStream_t stream) {
+  moe::DispatchDesc d;
+  d.x = x;
+  d.topk_idx = topk_idx;
+  d.topk_w = topk_w;
+  d.counts = counts;
+  d.offsets = offsets;
+  d.inv_pos = inv_pos;
+  d.row_token = row_token;
+  d.row_weight = row_weight;
+  d.xd = xd;
+  d.xd_scales = xd_scales;
+  d.scratch = hist_ptr(ws, L.l);
+  d.status = status_ptr(ws, L.l);
+  d.T = c->T;
+  d.h = c->h;
+  d.E = c->E;
+  d.k = c->k;
+  d.shared = c->I_shared > 0;
+  d.fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
+  cudaError_t e = moe::launch_dispatch(d, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  if (c->T > 0) counted(4);
+  return MOE_OK;
+}
+
+int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, const float* xd_scales,
+                  const int32_t* offsets, const float* row_weight, void* yd, void* ws, const Layout& L,
+                  cudaStream_t stream) {
+  if (c->dtype == MOE_DTYPE_FP8_BLOCK128) return fail(MOE_ERR_UNSUPPORTED, "the FP8 expert GEMM is not built yet");
+  (void)xd_scales;
+  if (c->T == 0) return MOE_OK;
+  const bool shared = c->I_shared > 0;
+  std::string err;
+  moe::GroupedGemmDesc g;
+  g.A = xd;
+  g.a_rows = L.R_tot;
+  g.B = w->w_gu;
+  g.Bs = shared ? w->w_gu_shared : nullptr;
+  g.b_rows = 2 * (int64_t)c->I;
+  g.offsets = offsets;
+  g.E = c->E;
+  g.R = (int)L.R;
+  g.T = c->T;
+  g.K = c->h;
+  g.N = 2 * c->I;
+  g.I = c->I;
+  g.mode = 0;
+  g.out = at<void>(ws, L.l.hbuf);
+  g.ldo = c->I;
+  g.row_weight = nullptr;
+  g.status = status_ptr(ws, L.l);
+  cudaError_t e = moe::launch_grouped_gemm_bf16(g, stream, &err);
+  if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "gate/up grouped GEMM launch") : cuda_fail(e, err.c_str());
+  g.A = at<void>(ws, L.l.hbuf);
+  g.B = w->w_d;
+  g.Bs = shared ? w->w_d_shared : nullptr;
+  g.b_rows = c->h;
+  g.K = c->I;
+  g.N = c->h;
+  g.mode = 1;
+  g.out = yd;
+  g.ldo = c->h;
+  g.row_weight = row_weight;
+  e = moe::launch_grouped_gemm_bf16(g, stream, &err);
+  if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "down grouped GEMM launch") : cuda_fail(e, err.c_str());
+  counted(2);
+  return MOE_OK;
+}
+
+int check_expert_weights(const moe_config* c, const moe_weights* w) {
+  if (!w) return fail(MOE_ERR_INVALID, "weights is NULL");
+  REQUIRE_PTR(w->w_gu, "weights->w_gu");
+  REQUIRE_PTR(w->w_d, "weights->w_d");
+  if (c->I_shared > 0) {
+    REQUIRE_PTR(w->w_gu_shared, "weights->w_gu_shared");
+    REQUIRE_PTR(w->w_d_shared, "weights->w_d_shared");
+  }
+  if (c->dtype == MOE_DTYPE_FP8_BLOCK128) {
+    REQUIRE_PTR(w->s_gu, "weights->s_gu");
+    REQUIRE_PTR(w->s_d, "weights->s_d");
+    if (c->I_shared > 0) {
+      REQUIRE_PTR(w->s_gu_shared, "weights->s_gu_shared");
+      REQUIRE_PTR(w->s_d_shared, "weights->s_d_shared");
+    }
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+MOE_EXPORT const char* moe_last_error(void) { return g_err.c_str(); }
+
+MOE_EXPORT uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+MOE_EXPORT int moe_workspace_layout(const moe_config* cfg, moe_ws_layout* layout) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!layout) return fail(MOE_ERR_INVALID, "layout is NULL");
+  *layout = make_layout(cfg).l;
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!bytes) return fail(MOE_ERR_INVALID, "bytes is NULL");
+  *bytes = make_layout(cfg).l.total;
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_route(const moe_config* cfg, const void* x, const moe_weights* weights, float* logits, int flags,
+                         int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (flags & ~MOE_LOGITS_GIVEN) return fail(MOE_ERR_INVALID, "unknown flags");
+  Layout L = make_layout(cfg);
+  if (flags & MOE_LOGITS_GIVEN) {
+    REQUIRE_PTR(logits, "logits (given)");
+  } else {
+    REQUIRE_PTR(x, "x");
+    if (!weights) return fail(MOE_ERR_INVALID, "weights is NULL");
+    REQUIRE_PTR(weights->w_router, "weights->w_router");
+    if (!logits) {
+      if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+      logits = at<float>(ws, L.l.logits);
+    } else if (!aligned16(logits)) {
+      return fail(MOE_ERR_INVALID, "logits must be 16-byte aligned");
+    }
+  }
+  if (cfg->score == MOE_SCORE_SIGMOID && weights && weights->bias && !aligned16(weights->bias))
+    return fail(MOE_ERR_INVALID, "weights->bias must be 16-byte aligned");
+  REQUIRE_PTR(topk_idx, "topk_idx");
+  REQUIRE_PTR(topk_w, "topk_w");
+  return do_route(cfg, x, weights, logits, flags, topk_idx, topk_w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_w,
+                            int32_t* counts, int32_t* offsets, int32_t* inv_pos, int32_t* row_token,
+                            float* row_weight, void* xd, float* xd_scales, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  Layout L = make_layout(cfg);
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  REQUIRE_PTR(x, "x");
+  REQUIRE_PTR(topk_idx, "topk_idx");
+  REQUIRE_PTR(topk_w, "topk_w");
+  REQUIRE_PTR(counts, "counts");
+  REQUIRE_PTR(offsets, "offsets");
+  REQUIRE_PTR(inv_pos, "inv_pos");
+  REQUIRE_PTR(row_token, "row_token");
+  REQUIRE_PTR(row_weight, "row_weight");
+  REQUIRE_PTR(xd, "xd");
+  if (cfg->dtype == MOE_DTYPE_FP8_BLOCK128) REQUIRE_PTR(xd_scales, "xd_scales");
+  return do_dispatch(cfg, x, topk_idx, topk_w, counts, offsets, inv_pos, row_token, row_weight, xd, xd_scales, ws, L,
+                     (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_expert_ffn(const moe_config* cfg, const moe_weights* weights, const void* xd,
+                              const float* xd_scales, const int32_t* offsets, const float* row_weight, void* yd,
+                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  Layout L = make_layout(cfg);
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  if ((rc = check_expert_weights(cfg, weights))) return rc;
+  REQUIRE_PTR(xd, "xd");
+  REQUIRE_PTR(offsets, "offsets");
+  REQUIRE_PTR(row_weight, "row_weight");
+  REQUIRE_PTR(yd, "yd");
+  if (cfg->dtype == MOE_DTYPE_FP8_BLOCK128) REQUIRE_PTR(xd_scales, "xd_scales");
+  return do_expert_ffn(cfg, weights, xd, xd_scales, offsets, row_weight, yd, ws, L, (cudaStream_t)stream);
+}
+
+MOE_EXPORT int moe_combine(const moe_config* cfg, const void* yd, const int32_t* inv_pos, void* y,
+                           moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  REQUIRE_PTR(yd, "yd");
+  REQUIRE_PTR(inv_pos, "inv_pos");
+  REQUIRE_PTR(y, "y");
+  cudaError_t e = moe::launch_combine(yd, inv_pos, y, cfg->T, cfg->h, cfg->k, cfg->I_shared > 0, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (cfg->T > 0) counted(1);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weights* weights, void* y, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  Layout L = make_layout(cfg);
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  REQUIRE_PTR(x, "x");
+  REQUIRE_PTR(y, "y");
+  if (!weights) return fail(MOE_ERR_INVALID, "weights is NULL");
+  REQUIRE_PTR(weights->w_router, "weights->w_router");
+  if ((rc = check_expert_weights(cfg, weights))) return rc;
+  if (cfg->dtype == MOE_DTYPE_FP8_BLOCK128) return fail(MOE_ERR_UNSUPPORTED, "the FP8 expert GEMM is not built yet");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(status_ptr(ws, L.l), 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  const moe_ws_layout& l = L.l;
+  if ((rc = do_route(cfg, x, weights, at<float>(ws, l.logits), 0, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w),
+                     s)))
+    return rc;
+  if ((rc = do_dispatch(cfg, x, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w), at<int32_t>(ws, l.counts),
+                        at<int32_t>(ws, l.offsets), at<int32_t>(ws, l.inv_pos), at<int32_t>(ws, l.row_token),
+                        at<float>(ws, l.row_weight), at<void>(ws, l.xd), at<float>(ws, l.xd_scales), ws, L, s)))
+    return rc;
+  if ((rc = do_expert_ffn(cfg, weights, at<void>(ws, l.xd), at<float>(ws, l.xd_scales), at<int32_t>(ws, l.offsets),
+                          at<float>(ws, l.row_weight), at<void>(ws, l.yd), ws, L, s)))
+    return rc;
+  e = moe::launch_combine(at<void>(ws, l.yd), at<int32_t>(ws, l.inv_pos), y, cfg->T, cfg->h, cfg->k,
+                          cfg->I_shared > 0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (cfg->T > 0) counted(1);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_quantize_weights_fp8(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, float* s,
+                                        moe_stream_t stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return fail(MOE_ERR_INVALID, "negative size");
+  if (rows % 128 || cols % 128) return fail(MOE_ERR_UNSUPPORTED, "rows and cols must be multiples of 128");
+  REQUIRE_PTR(w, "w");
+  REQUIRE_PTR(q, "q");
+  if (!s) return fail(MOE_ERR_INVALID, "s is NULL");
+  cudaError_t e = moe::launch_quantize_weights(w, batch, rows, cols, q, s, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "weight quantisation launch");
+  if (batch * (rows / 128) * (cols / 128) > 0) counted(1);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_device_status(const moe_config* cfg, void* ws, int32_t* status, moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!ws || !status) return fail(MOE_ERR_INVALID, "ws and status must not be NULL");
+  Layout L = make_layout(cfg);
+  int* p = status_ptr(ws, L.l);
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read-back");
+  *status = v;
+  if (v) return fail(MOE_ERR_DEVICE, "device status bits set: " + std::to_string(v));
+  return MOE_OK;
+}

@@ -1,0 +1,251 @@
+// Dispatch as a local permute.
+//
+// Perplexity "MoE Router": dense dispatch/combine needs the routing information aggregated per
+// expert rather than per token. Inference guide 6.4, section 3.1, step 2: each token's hidden state is
+// copied k times, once for each chosen expert. Perplexity "Quantization": activations are quantised
+// at run time per 1x128 vector (FP8 layer).
+//
+// Four kernels, all deterministic (integer atomics only, whose results do not depend on order):
+//   1. histogram   per 512-token block: counts of each expert      -> hist[block][E]
+//   2. scan        one CTA: per-expert running sum over blocks, exclusive scan over experts
+//                  -> counts, offsets, and the first row of every (block, expert)
+//   3. rank        per 512-token block: per-warp lane masks of each expert give every (token, slot)
+//                  its row, rows of an expert in ascending token order -> inv_pos, row_token,
+//                  row_weight
+//   4. gather      one warp per token: the token's row is read once and written to its k rows
+//                  (and to the shared expert's row), as bf16 or as e4m3 with 1x128 scales.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace dp {
+constexpr int TPB = 512;  // tokens per histogram / rank block
+constexpr int WARPS = TPB / 32;
+
+__global__ void __launch_bounds__(TPB) hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                   int32_t* __restrict__ hist, int* status) {
+  extern __shared__ int32_t sh[];
+  for (int e = threadIdx.x; e < E; e += TPB) sh[e] = 0;
+  __syncthreads();
+  const int64_t t = (int64_t)blockIdx.x * TPB + threadIdx.x;
+  if (t < T) {
+    bool bad = false;
+    for (int j = 0; j < k; ++j) {
+      int e = idx[t * k + j];
+      if (e >= 0 && e < E)
+        atomicAdd(&sh[e], 1);
+      else
+        bad = true;
+    }
+    if (bad) atomicOr(status, MOE_STATUS_BAD_EXPERT_INDEX);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += TPB) hist[(int64_t)blockIdx.x * E + e] = sh[e];
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nblk, int E,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_tot[32];
+  const int e = threadIdx.x;  // E <= 1024
+  int run = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      int c = hist[(int64_t)b * E + e];
+      hist[(int64_t)b * E + e] = run;
+      run += c;
+    }
+    counts[e] = run;
+  }
+  // exclusive scan of run over experts
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = warp_tot[lane];
+    int iv = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, iv, o);
+      if (lane >= o) iv += u;
+    }
+    warp_tot[lane] = iv - v;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = warp_tot[w] + incl - run;
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + run;
+  __syncthreads();
+  if (e < E)
+    for (int b = 0; b < nblk; ++b) hist[(int64_t)b * E + e] += excl;
+}
+
+__global__ void __launch_bounds__(TPB) rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+                                                   const int32_t* __restrict__ base, int T, int k, int E,
+                                                   int32_t* __restrict__ inv_pos, int32_t* __restrict__ row_token,
+                                                   float* __restrict__ row_weight) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* masks = smem;                                        // [WARPS][E]
+  int32_t* wbase = reinterpret_cast<int32_t*>(smem + WARPS * E);  // [WARPS][E]
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < WARPS * E; i += TPB) masks[i] = 0;
+  __syncthreads();
+  const int64_t t = (int64_t)blockIdx.x * TPB + threadIdx.x;
+  const bool tv = t < T;
+  if (tv)
+    for (int j = 0; j < k; ++j) {
+      int e = idx[t * k + j];
+      if (e >= 0 && e < E) atomicOr(&masks[w * E + e], 1u << lane);
+    }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += TPB) {
+    int run = base[(int64_t)blockIdx.x * E + e];
+    for (int ww = 0; ww < WARPS; ++ww) {
+      wbase[ww * E + e] = run;
+      run += __popc(masks[ww * E + e]);
+    }
+  }
+  __syncthreads();
+  if (tv) {
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      int e = idx[t * k + j];
+      int row = -1;
+      if (e >= 0 && e < E) {
+        row = wbase[w * E + e] + __popc(masks[w * E + e] & lt);
+        row_token[row] = (int32_t)t;
+        row_weight[row] = topk_w[t * k + j];
+      }
+      inv_pos[t * k + j] = row;
+    }
+  }
+}
+
+// one warp per token; lane covers 8 consecutive elements of every 256-element chunk
+__global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_pos,
+                                                          uint4* __restrict__ xd, int T, int h, int k, int R,
+                                                          int shared) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int hv = h / 8;  // uint4 per row
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const int my_row = lane < k ? inv_pos[(int64_t)t * k + lane] : -1;
+    const uint4* src = x + (int64_t)t * hv;
+    for (int c = lane; c < hv; c += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < hv) v[u] = src[c + 32 * u];
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (r < 0) continue;
+        uint4* dst = xd + (int64_t)r * hv;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c + 32 * u < hv) dst[c + 32 * u] = v[u];
+      }
+      if (shared) {
+        uint4* dst = xd + (int64_t)(R + t) * hv;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c + 32 * u < hv) dst[c + 32 * u] = v[u];
+      }
+    }
+  }
+}
+
+// FP8 variant: every 128-element block is quantised once (amax over 16 lanes), then its codes and
+// scale are written to the token's k rows (and the shared expert's row).
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_pos,
+                                                         uint8_t* __restrict__ xd, float* __restrict__ xs, int T, int h,
+                                                         int k, int R, int shared) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int hv = h / 8;
+  const int hb = h / 128;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const int my_row = lane < k ? inv_pos[(int64_t)t * k + lane] : -1;
+    const uint4* src = x + (int64_t)t * hv;
+    for (int c = lane; c < hv; c += 32) {  // 256 elements per pass: lanes 0-15 one block, 16-31 the next
+      uint4 v = src[c];
+      float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      uint32_t q[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t code = __nv_cvt_float_to_fp8(__fdiv_rn(f[i], scale), __NV_SATFINITE, __NV_E4M3);
+        q[i / 4] |= code << (8 * (i % 4));
+      }
+      const uint2 qv = make_uint2(q[0], q[1]);
+      const int blk = (c * 8) / 128;
+      const bool scale_writer = (lane & 15) == 0;
+      for (int j = 0; j <= k; ++j) {
+        int r;
+        if (j < k) {
+          r = __shfl_sync(0xffffffffu, my_row, j);
+          if (r < 0) continue;
+        } else {
+          if (!shared) break;
+          r = R + t;
+        }
+        *reinterpret_cast<uint2*>(xd + (int64_t)r * h + c * 8) = qv;
+        if (scale_writer) xs[(int64_t)r * hb + blk] = scale;
+      }
+    }
+  }
+}
+
+}  // namespace dp
+
+int dispatch_blocks(int T) { return (int)cdiv(T, dp::TPB); }
+size_t dispatch_scratch_ints(int T, int E) { return (size_t)dispatch_blocks(T) * (size_t)E; }
+
+cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
+  if (d.T == 0) {
+    // no tokens: offsets must still describe E empty experts
+    cudaError_t e = cudaMemsetAsync(d.counts, 0, sizeof(int32_t) * d.E, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d.offsets, 0, sizeof(int32_t) * (d.E + 1), stream);
+    return e;
+  }
+  const int nblk = dispatch_blocks(d.T);
+  dp::hist_kernel<<<nblk, dp::TPB, sizeof(int32_t) * d.E, stream>>>(d.topk_idx, d.T, d.k, d.E, d.scratch, d.status);
+  dp::scan_kernel<<<1, 1024, 0, stream>>>(d.scratch, nblk, d.E, d.counts, d.offsets);
+  const size_t rank_smem = sizeof(uint32_t) * 2 * dp::WARPS * d.E;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(dp::rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(uint32_t) * 2 * dp::WARPS * 1024));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dp::rank_kernel<<<nblk, dp::TPB, rank_smem, stream>>>(d.topk_idx, d.topk_w, d.scratch, d.T, d.k, d.E, d.inv_pos,
+                                                         d.row_token, d.row_weight);
+  int64_t blocks = cdiv(d.T, 8);
+  if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
+  const int R = d.T * d.k;
+  if (d.fp8)
+    dp::gather_fp8_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(d.x), d.inv_pos,
+                                                                reinterpret_cast<uint8_t*>(d.xd), d.xd_scales, d.T,
+                                                                d.h, d.k, R, d.shared);
+  else
+    dp::gather_bf16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(d.x), d.inv_pos,
+                                                                 reinterpret_cast<uint4*>(d.xd), d.T, d.h, d.k, R,
+                                                                 d.shared);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,450 @@
+// Grouped GEMM of the expert FFN on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Perplexity blog "Lower latency and higher throughput with multi-node DeepSeek deployment",
+// "Roofline model / GroupGEMM": g groups, group i multiplies [m_i, k] x [k, n]. Here the groups are
+// the E routed experts (rows [offsets[e], offsets[e+1]) of the expert-major buffer) plus the shared
+// expert (the last T rows), and the two projections of the SwiGLU FFN (inference guide 6.4,
+// section 2.1: gate, up, down) are two launches:
+//   mode 0  H  = silu(A W_gate^T) * (A W_up^T)     A = xd [R_tot, h], W_gu [E, 2I, h]
+//   mode 1  yd = (A W_down^T) * row_weight         A = H  [R_tot, I], W_d  [E, h, I]
+// Work follows the device-side per-expert counts (Perplexity, "Quantization": kernels read the
+// routing information to split the work, instead of sizing it from buffer bounds), so the launch
+// needs no host read-back and has a fixed grid.
+//
+// Design (GB300 / sm_103a):
+//   * persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ...; tile order is group-major,
+//     then output-column tile, then 128-row tile, so CTAs running together share the weight tile
+//     through L2 and an expert's activation rows stay L2-resident across its column tiles;
+//   * tile 128 x 256 x 64 (bf16), one tcgen05.mma.cta_group::1 M=128 N=256 K=16 per 32-byte K step;
+//   * warp 0 lane 0 issues TMA loads (128-byte swizzle) into a 4-stage shared-memory ring, warp 1
+//     lane 0 issues the MMAs, warps 2-5 drain the accumulator (TMEM, 2 x 256 columns, double
+//     buffered so the epilogue of one tile overlaps the MMAs of the next);
+//   * for mode 0 the B tile holds 128 gate rows and the 128 matching up rows, so the SwiGLU product
+//     is formed in the epilogue and only H is written;
+//   * every mbarrier wait is bounded; on a time-out the kernel records MOE_STATUS_WAIT_TIMEOUT,
+//     drains its own copies and MMAs (again bounded), frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace gg {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int MAX_GROUPS = 1025;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+
+struct Args {
+  const int32_t* offsets;  // [E + 1]
+  int E;
+  int shared;  // 1: group E is the shared expert (rows [R, R + T))
+  int R;
+  int T;
+  int K;        // reduction length (multiple of BK)
+  int n_tiles;  // output column tiles per group
+  int mode;     // 0: gate/up + SwiGLU -> H; 1: down * row_weight -> yd
+  int I;        // mode 0: row offset of the up half inside W_gu
+  int ldo;      // output row stride in elements
+  void* out;
+  const float* row_weight;
+  int* status;
+  long long wait_limit;
+};
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_slot;
+  volatile int abort_flag;
+  int gtile[MAX_GROUPS + 1];  // exclusive prefix of 128-row tiles per group
+  int grow[MAX_GROUPS + 1];   // first row of each group (and the end row)
+};
+
+__device__ __forceinline__ bool wait_or_abort(Shared& s, uint64_t* bar, uint32_t parity, const Args& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (s.abort_flag) return false;
+    if (clock64() - t0 > a.wait_limit) {
+      s.abort_flag = 1;
+      atomicOr(a.status, MOE_STATUS_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+struct Tile {
+  int g, m_tile, n_tile, a_row, rows;
+};
+
+__device__ __forceinline__ Tile decode(const Shared& s, int G, int n_tiles, int tile) {
+  int q = tile / n_tiles;
+  int lo = 0, hi = G - 1;  // last g with gtile[g] <= q
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (s.gtile[mid] <= q)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  Tile t;
+  t.g = lo;
+  int local = tile - s.gtile[lo] * n_tiles;
+  int mtc = s.gtile[lo + 1] - s.gtile[lo];
+  t.n_tile = local / mtc;
+  t.m_tile = local - t.n_tile * mtc;
+  t.a_row = s.grow[lo] + t.m_tile * BM;
+  int m = s.grow[lo + 1] - s.grow[lo];
+  t.rows = min(BM, m - t.m_tile * BM);
+  return t;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmBs, const Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared s;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.E + args.shared;
+
+  // ---- set-up: tile prefix over groups, barriers, TMEM
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      int g = base + lane;
+      int row0 = 0, m = 0;
+      if (g < G) {
+        if (g < args.E) {
+          row0 = args.offsets[g];
+          m = args.offsets[g + 1] - row0;
+        } else {
+          row0 = args.R;
+          m = args.T;
+        }
+      }
+      int mt = (m + BM - 1) / BM;
+      int incl = mt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < G) {
+        s.gtile[g] = carry + incl - mt;
+        s.grow[g] = row0;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s.gtile[G] = carry;
+      s.grow[G] = args.shared ? args.R + args.T : args.offsets[args.E];
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(&s.full[i], 1);
+        mbar_init(&s.empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&s.tfull[i], 1);
+        mbar_init(&s.tempty[i], 4);
+      }
+      mbar_init(&s.mma_done, 1);
+      s.abort_flag = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmBs);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_slot;
+  const int total = s.gtile[G] * args.n_tiles;
+  const int kblocks = args.K / BK;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      Tile t = decode(s, G, args.n_tiles, tile);
+      const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
+      int z = t.g < args.E ? t.g : 0;
+      int n0, n1;
+      if (args.mode == 0) {
+        n0 = t.n_tile * (BN / 2);
+        n1 = args.I + t.n_tile * (BN / 2);
+      } else {
+        n0 = t.n_tile * BN;
+        n1 = n0 + BN / 2;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(s, &s.empty[stage], phase ^ 1, args)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = smem + stage * STAGE_BYTES;
+        uint8_t* b = a + A_BYTES;
+        mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
+        tma_load_2d(a, &tmA, &s.full[stage], kb * BK, t.a_row);
+        tma_load_3d(b, mb, &s.full[stage], kb * BK, n0, z);
+        tma_load_3d(b + B_BYTES / 2, mb, &s.full[stage], kb * BK, n1, z);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // drain: the last fills of every stage must have landed before the CTA may exit
+    long long first = issued > STAGES ? issued - STAGES : 0;
+    for (long long i = first; i < issued; ++i) {
+      int st = (int)(i % STAGES);
+      uint32_t ph = (uint32_t)((i / STAGES) & 1);
+      long long t0 = clock64();
+      while (!mbar_try_wait(&s.full[st], ph) && clock64() - t0 < args.wait_limit) {
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (!wait_or_abort(s, &s.tempty[acc], acc_phase ^ 1, args)) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(s, &s.full[stage], phase, args)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t b = a + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_f16(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), IDESC, (kb | kk) != 0);
+        umma_commit(&s.empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      umma_commit(&s.tfull[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    // all MMAs issued by this thread complete before TMEM / shared memory go away
+    umma_commit(&s.mma_done);
+    long long t0 = clock64();
+    while (!mbar_try_wait(&s.mma_done, 0) && clock64() - t0 < args.wait_limit) {
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> registers -> global
+    const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32)
+    const int r = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      Tile t = decode(s, G, args.n_tiles, tile);
+      // one lane waits, the warp follows: the tcgen05.ld below is warp-collective
+      int ok = 1;
+      if (lane == 0) ok = wait_or_abort(s, &s.tfull[acc], acc_phase, args);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
+      tc_fence_after();
+      const bool valid = r < t.rows;
+      const int64_t orow = (int64_t)t.a_row + r;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      if (args.mode == 0) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c, g);
+          tmem_ld32(taddr + BN / 2 + c, u);
+          tmem_ld_wait();
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+            float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+            p[i] = pack_bf16x2(h0, h1);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          }
+        }
+      } else {
+        const float w = (valid && t.g < args.E) ? args.row_weight[orow] : 1.0f;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            p[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * w, __uint_as_float(v[2 * i + 1]) * w);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace gg
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// [rows, K] row-major matrix of `elem`-byte elements; box = box_rows x (128 bytes of K).
+bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t rows, int64_t K,
+               int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K * elem)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [G, rows, K] row-major stack of matrices; box = 1 x box_rows x (128 bytes of K).
+bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t G, int64_t rows,
+               int64_t K, int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)G};
+  cuuint64_t strides[2] = {(cuuint64_t)(K * elem), (cuuint64_t)(rows * K * elem)};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMsHint;
+  }
+  return n;
+}
+
+cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return e;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gg::SMEM_BYTES);
+    if (e != cudaSuccess) {
+      *err = "cudaFuncSetAttribute failed";
+      return e;
+    }
+    attr_set = true;
+  }
+  CUtensorMap tA, tB, tBs;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = encode_2d(&tA, d.A, BF, 2, d.a_rows, d.K, gg::BM) &&
+            encode_3d(&tB, d.B, BF, 2, d.E, d.b_rows, d.K, gg::BN / 2) &&
+            encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, gg::BN / 2);
+  if (!ok) {
+    *err = "cuTensorMapEncodeTiled rejected a grouped-GEMM operand";
+    return cudaErrorInvalidValue;
+  }
+  gg::Args a;
+  a.offsets = d.offsets;
+  a.E = d.E;
+  a.shared = d.Bs != nullptr;
+  a.R = d.R;
+  a.T = d.T;
+  a.K = d.K;
+  a.mode = d.mode;
+  a.I = d.I;
+  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : d.N / gg::BN;
+  a.ldo = d.ldo;
+  a.out = d.out;
+  a.row_weight = d.row_weight;
+  a.status = d.status;
+  a.wait_limit = 4000000000LL;  // about two seconds of SM clock
+  gg::grouped_gemm_bf16_kernel<<<num_sms(), gg::THREADS, gg::SMEM_BYTES, stream>>>(tA, tB, tBs, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

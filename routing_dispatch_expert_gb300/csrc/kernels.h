@@ -1,0 +1,75 @@
+// Internal launchers of the sm_103a kernels (host side). Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace moe {
+
+int num_sms();
+
+// Step 1: router GEMM, logits[T, E] = x[T, h] (bf16) . w_r[E, h]^T (fp32), fp32 accumulation.
+cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, int T, int h, int E,
+                               cudaStream_t stream);
+
+// Step 1: top-k selection and route weights from fp32 logits, one warp per token.
+struct TopkDesc {
+  const float* logits;
+  const float* bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  int T, E, k, n_group, topk_group, score, renorm;
+  float routed_scale;
+};
+cudaError_t launch_topk(const TopkDesc& d, cudaStream_t stream);
+
+// Steps 2-3: per-block histogram, scan, stable ranks, and the dispatch copy.
+int dispatch_blocks(int T);  // token blocks of the histogram / rank kernels
+size_t dispatch_scratch_ints(int T, int E);
+struct DispatchDesc {
+  const void* x;
+  const int32_t* topk_idx;
+  const float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* inv_pos;
+  int32_t* row_token;
+  float* row_weight;
+  void* xd;
+  float* xd_scales;
+  int32_t* scratch;  // dispatch_scratch_ints(T, E) ints
+  int* status;
+  int T, h, E, k;
+  int shared;  // also write the T token rows for the shared expert
+  int fp8;
+};
+cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream);
+
+// Step 3: grouped GEMM (tcgen05) of one projection.
+struct GroupedGemmDesc {
+  const void* A;  // [a_rows, K]
+  int64_t a_rows;
+  const void* B;   // [E, b_rows, K]
+  const void* Bs;  // [b_rows, K] shared expert or nullptr
+  int64_t b_rows;
+  const int32_t* offsets;
+  int E, R, T, K, N, I;
+  int mode;  // 0 gate/up -> H, 1 down -> yd
+  void* out;
+  int ldo;
+  const float* row_weight;
+  int* status;
+};
+cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
+
+// Step 4: combine.
+cudaError_t launch_combine(const void* yd, const int32_t* inv_pos, void* y, int T, int h, int k, int shared,
+                           cudaStream_t stream);
+
+// Static weight quantisation, 128x128 tiles.
+cudaError_t launch_quantize_weights(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, float* s,
+                                    cudaStream_t stream);
+
+}  // namespace moe

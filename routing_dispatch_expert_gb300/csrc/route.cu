@@ -1,0 +1,298 @@
+// Step 1 of the layer: router scores and top-k selection.
+//
+// Ultralytics glossary "Expert Parallelism", "How tokens move across GPUs", step 1: the router
+// scores every token against every expert and keeps the k best. TensorRT-LLM "DeepSeek R1
+// throughput on Blackwell", "RouterGEMM mixed I/O": bf16 activations in, fp32 logits out, no cast
+// kernel; "Top-K kernel fusion": groups first, then the top experts inside them, with a bias and a
+// scaling factor, as one fused kernel. Perplexity "MoE Router": Mixtral routing is the special case
+// top-k-group = all groups; the sparse kernels consume indices and scores directly.
+//
+// Readings where the pages are silent: the group score is the sum of the two largest biased scores
+// of the group; ties go to the lower expert (and group) index; the sigmoid is evaluated in fp64 and
+// rounded once to fp32, and the selection key is that fp32 value plus the bias in fp32, so the
+// selection is a deterministic function of the fp32 logits; softmax layers select on the logits.
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------
+// router GEMM: logits[T, E] = x[T, h] . w_r[E, h]^T on the CUDA cores in fp32 (bf16 x read
+// directly, converted in registers). 128 x 128 output tile per CTA, 8 x 8 per thread, K step 16,
+// register-staged double buffering.
+// ------------------------------------------------------------------------------------------
+namespace rg {
+constexpr int BM = 128, BN = 128, BK = 16, PAD = 4, THREADS = 256;
+
+__global__ void __launch_bounds__(THREADS) router_gemm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                              const float* __restrict__ w, float* __restrict__ out,
+                                                              int T, int h, int E) {
+  __shared__ __align__(16) float As[2][BK][BM + PAD];
+  __shared__ __align__(16) float Bs[2][BK][BN + PAD];
+  const int tid = threadIdx.x;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int ty = tid / 16, tx = tid % 16;
+
+  // global -> register staging
+  const int a_row = tid / 2, a_k = (tid % 2) * 8;
+  const bool a_ok = m0 + a_row < T;
+  const __nv_bfloat16* a_src = x + (int64_t)(m0 + a_row) * h + a_k;
+  int b_row[2], b_k[2];
+  bool b_ok[2];
+  const float* b_src[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    int idx = tid + THREADS * p;
+    b_row[p] = idx / 4;
+    b_k[p] = (idx % 4) * 4;
+    b_ok[p] = n0 + b_row[p] < E;
+    b_src[p] = w + (int64_t)(n0 + b_row[p]) * h + b_k[p];
+  }
+  uint4 ra;
+  float4 rb[2];
+  auto load = [&](int k0) {
+    ra = a_ok ? *reinterpret_cast<const uint4*>(a_src + k0) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+      rb[p] = b_ok[p] ? *reinterpret_cast<const float4*>(b_src[p] + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto store = [&](int buf) {
+    const uint32_t av[4] = {ra.x, ra.y, ra.z, ra.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      As[buf][a_k + 2 * i][a_row] = bf16_lo(av[i]);
+      As[buf][a_k + 2 * i + 1][a_row] = bf16_hi(av[i]);
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      Bs[buf][b_k[p] + 0][b_row[p]] = rb[p].x;
+      Bs[buf][b_k[p] + 1][b_row[p]] = rb[p].y;
+      Bs[buf][b_k[p] + 2][b_row[p]] = rb[p].z;
+      Bs[buf][b_k[p] + 3][b_row[p]] = rb[p].w;
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  load(0);
+  store(0);
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = 0; k0 < h; k0 += BK) {
+    const bool more = k0 + BK < h;
+    if (more) load(k0 + BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[8], b[8];
+      *reinterpret_cast<float4*>(a) = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+      *reinterpret_cast<float4*>(a + 4) = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+      *reinterpret_cast<float4*>(b) = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+      *reinterpret_cast<float4*>(b + 4) = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (more) {
+      store(buf ^ 1);
+      __syncthreads();
+      buf ^= 1;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int row = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    if (row >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int col = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+      if (col < E) out[(int64_t)row * E + col] = acc[i][j];
+    }
+  }
+}
+}  // namespace rg
+
+cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, int T, int h, int E,
+                               cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  dim3 grid((unsigned)cdiv(T, rg::BM), (unsigned)cdiv(E, rg::BN));
+  rg::router_gemm_kernel<<<grid, rg::THREADS, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(x), w_r, logits,
+                                                            T, h, E);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// top-k: one warp per token; lane l holds experts [l * EPL, l * EPL + EPL).
+// ------------------------------------------------------------------------------------------
+namespace tk {
+
+// argmax over the warp: larger value wins, equal values go to the lower expert index
+__device__ __forceinline__ void warp_argmax(float& v, int& e, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oe = __shfl_xor_sync(0xffffffffu, e, o);
+    float os = __shfl_xor_sync(0xffffffffu, s, o);
+    if (ov > v || (ov == v && oe < e)) {
+      v = ov;
+      e = oe;
+      s = os;
+    }
+  }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int gs = d.E / d.n_group;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.T; t += warps) {
+    const float* lrow = d.logits + (int64_t)t * d.E;
+    float key[EPL], sv[EPL];
+    bool valid[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane * EPL + i;
+      valid[i] = e < d.E;
+      float l = valid[i] ? lrow[e] : 0.f;
+      float s, kv;
+      if (d.score == MOE_SCORE_SOFTMAX) {
+        s = l;
+        kv = l;
+      } else {
+        s = __double2float_rn(1.0 / (1.0 + exp(-(double)l)));
+        kv = d.bias ? __fadd_rn(s, d.bias[valid[i] ? e : 0]) : s;
+      }
+      if (kv != kv) kv = -INFINITY;  // NaN never wins
+      sv[i] = s;
+      key[i] = valid[i] ? kv : -INFINITY;
+    }
+
+    // group stage
+    uint32_t kept = 0xffffffffu;
+    if (d.n_group > 1) {
+      float my_gscore = -INFINITY;
+      for (int g = 0; g < d.n_group; ++g) {
+        float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane * EPL + i;
+          if (valid[i] && e / gs == g) {
+            float v = key[i];
+            if (v > t1) {
+              t2 = t1;
+              t1 = v;
+            } else if (v > t2) {
+              t2 = v;
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+          float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+          float n1 = fmaxf(t1, o1);
+          t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+          t1 = n1;
+        }
+        float sc = gs >= 2 ? __fadd_rn(t1, t2) : t1;
+        if (lane == g) my_gscore = sc;
+      }
+      kept = 0;
+      for (int r = 0; r < d.topk_group; ++r) {
+        bool cand = lane < d.n_group && !((kept >> lane) & 1u);
+        float v = cand ? my_gscore : -INFINITY;
+        int gi = cand ? lane : 64 + lane;
+        float dummy = 0.f;
+        warp_argmax(v, gi, dummy);
+        kept |= 1u << (gi & 31);
+      }
+    }
+
+    // expert stage
+    uint32_t taken = 0;
+    int sel_e = 0;
+    float sel_s = 0.f;
+    for (int j = 0; j < d.k; ++j) {
+      float bv = -INFINITY, bs = 0.f;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane * EPL + i;
+        const bool ok = valid[i] && !((taken >> i) & 1u) && ((kept >> (e / gs)) & 1u);
+        if (ok && (key[i] > bv || be == 0x7fffffff)) {
+          bv = key[i];
+          be = e;
+          bs = sv[i];
+        }
+      }
+      warp_argmax(bv, be, bs);
+      if (be / EPL == lane) taken |= 1u << (be - lane * EPL);
+      if (lane == j) {
+        sel_e = be;
+        sel_s = bs;
+      }
+    }
+
+    // route weights
+    double w = 0.0;
+    if (d.score == MOE_SCORE_SOFTMAX) {
+      float lmax = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (valid[i]) lmax = fmaxf(lmax, sv[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+      double z = 0.0;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (valid[i]) z += exp((double)sv[i] - (double)lmax);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (lane < d.k) w = exp((double)sel_s - (double)lmax) / z;
+    } else {
+      if (lane < d.k) w = (double)sel_s;
+    }
+    if (d.renorm) {
+      double sum = lane < d.k ? w : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      w = w / sum;
+    }
+    if (lane < d.k) {
+      d.topk_idx[(int64_t)t * d.k + lane] = sel_e;
+      d.topk_w[(int64_t)t * d.k + lane] = (float)(w * (double)d.routed_scale);
+    }
+  }
+}
+
+}  // namespace tk
+
+cudaError_t launch_topk(const TopkDesc& d, cudaStream_t stream) {
+  if (d.T == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = cdiv(d.T, threads / 32);
+  if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
+  const int epl = (d.E + 31) / 32;
+  if (epl <= 1)
+    tk::topk_kernel<1><<<(unsigned)blocks, threads, 0, stream>>>(d);
+  else if (epl <= 2)
+    tk::topk_kernel<2><<<(unsigned)blocks, threads, 0, stream>>>(d);
+  else if (epl <= 4)
+    tk::topk_kernel<4><<<(unsigned)blocks, threads, 0, stream>>>(d);
+  else if (epl <= 8)
+    tk::topk_kernel<8><<<(unsigned)blocks, threads, 0, stream>>>(d);
+  else if (epl <= 16)
+    tk::topk_kernel<16><<<(unsigned)blocks, threads, 0, stream>>>(d);
+  else
+    tk::topk_kernel<32><<<(unsigned)blocks, threads, 0, stream>>>(d);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

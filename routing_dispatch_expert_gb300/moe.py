@@ -1,0 +1,208 @@
+"""Python binding of libmoe_gb300.so (include/moe.h): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module converts torch tensors to
+device pointers, passes the current CUDA stream, and raises ``MoeError`` on a non-zero status.
+There is no fallback: if the library is not built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+SO_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
+MOE_DTYPE_BF16, MOE_DTYPE_FP8_BLOCK128 = 0, 1
+MOE_LOGITS_GIVEN = 1
+MOE_STATUS_BAD_EXPERT_INDEX, MOE_STATUS_WAIT_TIMEOUT = 1, 2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("h", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("score", ctypes.c_int32), ("renormalize", ctypes.c_int32),
+                ("routed_scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class MoeWeightsStruct(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_router", "bias", "w_gu", "s_gu", "w_d", "s_d", "w_gu_shared",
+                                               "s_gu_shared", "w_d_shared", "s_d_shared")]
+
+
+class MoeWsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "inv_pos",
+                                               "row_token", "row_weight", "xd", "xd_scales", "hbuf", "h_scales", "yd",
+                                               "scratch", "total")]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load():
+    """Load the CUDA library (built by ``routing_dispatch_expert_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(SO_PATH):
+                raise ImportError(f"libmoe_gb300.so is not built ({SO_PATH}); run routing_dispatch_expert_gb300.build")
+            L = ctypes.CDLL(SO_PATH)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            cfgp = ctypes.POINTER(MoeConfig)
+            wp = ctypes.POINTER(MoeWeightsStruct)
+            sig = {
+                "moe_workspace_size": [cfgp, ctypes.POINTER(sz)],
+                "moe_workspace_layout": [cfgp, ctypes.POINTER(MoeWsLayout)],
+                "moe_route": [cfgp, vp, wp, vp, i32, vp, vp, vp, sz, vp],
+                "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                "moe_expert_ffn": [cfgp, wp, vp, vp, vp, vp, vp, vp, sz, vp],
+                "moe_combine": [cfgp, vp, vp, vp, vp],
+                "moe_forward": [cfgp, vp, wp, vp, vp, sz, vp],
+                "moe_quantize_weights_fp8": [vp, i64, i64, i64, vp, vp, vp],
+                "moe_device_status": [cfgp, vp, ctypes.POINTER(ctypes.c_int32), vp],
+            }
+            for name, args in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = i32
+            L.moe_last_error.argtypes = []
+            L.moe_last_error.restype = ctypes.c_char_p
+            L.moe_launch_count.argtypes = []
+            L.moe_launch_count.restype = ctypes.c_uint64
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        raise MoeError(rc, load().moe_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def make_config(T, h, E, k, I, I_shared=0, n_group=1, topk_group=1, score="softmax", renorm=False, routed_scale=1.0,
+                dtype="bf16") -> MoeConfig:
+    return MoeConfig(T, h, E, k, I, I_shared, n_group, topk_group,
+                     MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID, int(bool(renorm)),
+                     float(routed_scale), MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP8_BLOCK128)
+
+
+class Weights:
+    """Device tensors of one layer and their C struct. bf16 expert weights for dtype 'bf16'; for
+    'fp8' pass e4m3 codes (torch.uint8) and fp32 128x128 scales (see quantize_weights_fp8)."""
+
+    def __init__(self, w_router, bias=None, w_gu=None, w_d=None, w_gu_shared=None, w_d_shared=None, s_gu=None,
+                 s_d=None, s_gu_shared=None, s_d_shared=None):
+        self.tensors = dict(w_router=w_router, bias=bias, w_gu=w_gu, s_gu=s_gu, w_d=w_d, s_d=s_d,
+                            w_gu_shared=w_gu_shared, s_gu_shared=s_gu_shared, w_d_shared=w_d_shared,
+                            s_d_shared=s_d_shared)
+        self.struct = MoeWeightsStruct(**{n: (None if t is None else t.data_ptr()) for n, t in self.tensors.items()})
+
+
+def workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t()
+    _check(load().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def workspace_layout(cfg: MoeConfig) -> dict:
+    l = MoeWsLayout()
+    _check(load().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(l)))
+    return {n: getattr(l, n) for n, _ in MoeWsLayout._fields_}
+
+
+def alloc_workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
+    return torch.empty(workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def ws_view(ws: torch.Tensor, cfg: MoeConfig, name: str, dtype, shape) -> torch.Tensor:
+    """A typed view of one intermediate inside a moe_forward workspace."""
+    off = workspace_layout(cfg)[name]
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype).view(*shape)
+
+
+def route(cfg, x, weights: Weights | None, topk_idx, topk_w, logits=None, logits_given=False, ws=None):
+    _check(load().moe_route(ctypes.byref(cfg), _ptr(x), None if weights is None else ctypes.byref(weights.struct),
+                            _ptr(logits), MOE_LOGITS_GIVEN if logits_given else 0, _ptr(topk_idx), _ptr(topk_w),
+                            _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+
+
+def dispatch(cfg, x, topk_idx, topk_w, counts, offsets, inv_pos, row_token, row_weight, xd, xd_scales, ws):
+    _check(load().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(offsets),
+                               _ptr(inv_pos), _ptr(row_token), _ptr(row_weight), _ptr(xd), _ptr(xd_scales), _ptr(ws),
+                               ws.numel(), _stream()))
+
+
+def expert_ffn(cfg, weights: Weights, xd, xd_scales, offsets, row_weight, yd, ws):
+    _check(load().moe_expert_ffn(ctypes.byref(cfg), ctypes.byref(weights.struct), _ptr(xd), _ptr(xd_scales),
+                                 _ptr(offsets), _ptr(row_weight), _ptr(yd), _ptr(ws), ws.numel(), _stream()))
+
+
+def combine(cfg, yd, inv_pos, y):
+    _check(load().moe_combine(ctypes.byref(cfg), _ptr(yd), _ptr(inv_pos), _ptr(y), _stream()))
+
+
+def forward(cfg, x, weights: Weights, y, ws):
+    _check(load().moe_forward(ctypes.byref(cfg), _ptr(x), ctypes.byref(weights.struct), _ptr(y), _ptr(ws), ws.numel(),
+                              _stream()))
+
+
+def quantize_weights_fp8(w: torch.Tensor):
+    """Static 128x128 quantisation of bf16 weights [..., rows, cols] -> (e4m3 codes uint8, fp32 scales)."""
+    rows, cols = w.shape[-2], w.shape[-1]
+    batch = w.numel() // (rows * cols)
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    s = torch.empty(tuple(w.shape[:-2]) + (rows // 128, cols // 128), dtype=torch.float32, device=w.device)
+    _check(load().moe_quantize_weights_fp8(_ptr(w), batch, rows, cols, _ptr(q), _ptr(s), _stream()))
+    return q, s
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().moe_launch_count())
+
+
+def device_status(cfg, ws) -> int:
+    v = ctypes.c_int32()
+    rc = load().moe_device_status(ctypes.byref(cfg), _ptr(ws), ctypes.byref(v), _stream())
+    if rc not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(rc)
+    return v.value
+
+
+class MoeLayer:
+    """Convenience wrapper: a config, its weights and a workspace; ``layer(x)`` runs moe_forward."""
+
+    def __init__(self, cfg: MoeConfig, weights: Weights, device="cuda"):
+        self.cfg = cfg
+        self.weights = weights
+        self.ws = alloc_workspace(cfg, device)
+        # a fresh workspace holds arbitrary bits in its status word; read-and-clear it once
+        device_status(cfg, self.ws)
+
+    def __call__(self, x: torch.Tensor, y: torch.Tensor | None = None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty_like(x)
+        forward(self.cfg, x, self.weights, y, self.ws)
+        return y

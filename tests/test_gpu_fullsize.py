@@ -1,0 +1,115 @@
+"""CUDA path vs the oracle at the full sizes of the measured workloads, in the launch configuration
+the bench times (moe_forward): full routing and permutation bit-exact, sampled dispatch rows
+bit-exact, sampled router logits and sampled token outputs within tolerance."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import routing_dispatch_expert_gb300 as rde
+from routing_dispatch_expert_gb300 import build as pkg_build
+from harness import BF16_TOL, GpuLayer, bits, cfg_of, oracle_tokens, rel_err_per_token, route_kwargs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkg_build.build()
+    synth.build()
+    rde.load()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _sample(n, count, seed):
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(n, size=min(count, n), replace=False).tolist())
+    s.update({0, n - 1})
+    return np.array(sorted(s))
+
+
+@pytest.mark.parametrize("name,n_tok", [("mixtral", 4), ("dsv3_prefill", 8), ("dsv3_decode", 16)])
+def test_full_size_layer(name, n_tok):
+    wl = synth.WORKLOADS[name]
+    L = GpuLayer(wl)
+    y = L.forward()
+    assert rde.device_status(L.cfg, L.ws) == 0
+    it = L.intermediates()
+    x = bits(L.inp["x"])
+    bias = None if L.inp["bias"] is None else L.inp["bias"].cpu().numpy()
+    logits = it["logits"].cpu().numpy()
+    # routing of every token, from the same logits: bit-exact indices
+    idx, w = oracle.route(logits, bias, **route_kwargs(wl))
+    np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), idx)
+    np.testing.assert_allclose(it["topk_w"].cpu().numpy(), w, rtol=1e-6, atol=1e-7)
+    # aggregation and permutation of every row: bit-exact
+    counts, offsets, inv_pos, row_token = oracle.permute(idx, wl.E)
+    np.testing.assert_array_equal(it["counts"].cpu().numpy(), counts)
+    np.testing.assert_array_equal(it["offsets"].cpu().numpy(), offsets)
+    np.testing.assert_array_equal(it["inv_pos"].cpu().numpy(), inv_pos)
+    np.testing.assert_array_equal(it["row_token"].cpu().numpy(), row_token)
+    # dispatch copies of sampled rows: bit-exact
+    R = wl.T * wl.k
+    rows = _sample(R, 512, 1)
+    np.testing.assert_array_equal(bits(it["xd"][torch.as_tensor(rows, device="cuda")]), x[row_token[rows]])
+    # router GEMM on sampled tokens vs the fp64 oracle
+    toks = _sample(wl.T, 32, 2)
+    lo = oracle.router_logits(x[toks], L.inp["w_router"].cpu().numpy())
+    assert np.abs(logits[toks] - lo).max() <= 1e-5 * np.abs(lo).max() + 1e-6
+    # layer output of sampled tokens (experts evaluated by the oracle one at a time)
+    toks = _sample(wl.T, n_tok, 3)
+    y_ref, o, _ = oracle_tokens(L, toks, idx, w, x)
+    e = rel_err_per_token(bits(y[torch.as_tensor(toks, device="cuda")]), y_ref)
+    assert e.max() <= BF16_TOL, f"max rel err {e.max()}"
+    # the route-weighted expert rows of those tokens
+    yd = oracle.bf16_to_double(bits(it["yd"][torch.as_tensor(inv_pos[toks].ravel(), device="cuda")]))
+    ref = (o * w[toks][:, :, None].astype(np.float64)).reshape(-1, wl.h)
+    err = np.abs(yd - ref).max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-30)
+    assert err.max() <= BF16_TOL
+    del L
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_full_size_fp8_routing_and_dispatch():
+    """The FP8 layer's routing, permutation and 1x128 activation quantisation at full size."""
+    wl = synth.WORKLOADS["dsv3_fp8"]
+    cfg = cfg_of(wl)
+    inp = synth.device_inputs(wl, torch, with_weights=False)
+    T, k, E, h = wl.T, wl.k, wl.E, wl.h
+    dev = "cuda"
+    ws = rde.alloc_workspace(cfg)
+    rde.device_status(cfg, ws)
+    w_only = rde.Weights(w_router=inp["w_router"], bias=inp["bias"])
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    rde.route(cfg, inp["x"], w_only, idx, w, logits=logits, ws=ws)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty(T, k, dtype=torch.int32, device=dev)
+    row_token = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_weight = torch.empty(T * k, dtype=torch.float32, device=dev)
+    xd = torch.empty(T * k + T, h, dtype=torch.uint8, device=dev)
+    xs = torch.empty(T * k + T, h // 128, dtype=torch.float32, device=dev)
+    rde.dispatch(cfg, inp["x"], idx, w, counts, offsets, inv_pos, row_token, row_weight, xd, xs, ws)
+    assert rde.device_status(cfg, ws) == 0
+    ri, rw = oracle.route(logits.cpu().numpy(), inp["bias"].cpu().numpy(), **route_kwargs(wl))
+    np.testing.assert_array_equal(idx.cpu().numpy(), ri)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+    c, off, ip, rt = oracle.permute(ri, E)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), off)
+    np.testing.assert_array_equal(inv_pos.cpu().numpy(), ip)
+    # Zipf(1.0) skew: the hottest expert takes far more than the mean
+    assert c.max() > 8 * c.mean()
+    rows = _sample(T * k, 256, 4)
+    x = bits(inp["x"])
+    xq, xsc = oracle.quant_1x128(oracle.bf16_to_double(x[rt[rows]]))
+    sel = torch.as_tensor(rows, device=dev)
+    np.testing.assert_array_equal(xd[sel].cpu().numpy(), xq)
+    np.testing.assert_array_equal(xs[sel].cpu().numpy(), xsc)

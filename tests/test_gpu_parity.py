@@ -1,0 +1,263 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded inputs at sizes the oracle finishes in
+seconds (several tiles and ragged tails). Every call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import routing_dispatch_expert_gb300 as rde
+from routing_dispatch_expert_gb300 import build as pkg_build
+from harness import (BF16_TOL, MARGIN, GpuLayer, bits, cfg_of, oracle_tokens, rel_err_per_token, route_kwargs,
+                     selection_margin)
+
+pytestmark = pytest.mark.gpu
+
+_W = synth.WORKLOADS
+SMALL = {
+    "tiny": _W["tiny"],  # the full tiny layer: 4096 tokens, h 512, 8 experts, top-2
+    "mixtral_small": _W["mixtral"].replace(name="mixtral_small", T=300, h=512, I=384),
+    "dsv3_small": _W["dsv3_prefill"].replace(name="dsv3_small", T=500, h=512, E=64, I=256, I_shared=256),
+    "dsv3_small_noshared": _W["dsv3_prefill"].replace(name="dsv3_small_noshared", T=129, h=256, E=32, I=128,
+                                                      I_shared=0),
+    "dsv3_skew": _W["dsv3_decode"].replace(name="dsv3_skew", T=77, h=512, E=64, I=256, I_shared=256),
+    "dsv3_hot": _W["dsv3_decode"].replace(name="dsv3_hot", T=400, h=256, E=64, I=128, I_shared=128, zipf_s=6.0),
+    "single_token": _W["dsv3_prefill"].replace(name="single_token", T=1, h=256, E=64, I=128, I_shared=128),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkg_build.build()
+    synth.build()
+    rde.load()
+
+
+def test_device_generator_matches_host_generator():
+    t = synth.device_normal_bf16(torch, (1000, 37), 5, synth.STREAM_WGU, 0.02, offset=123)
+    np.testing.assert_array_equal(bits(t).ravel(), synth.normal_bf16(5, synth.STREAM_WGU, 123, 37000, 0.02))
+    mu = np.linspace(-1, 1, 37).astype(np.float32)
+    t = synth.device_normal_bf16(torch, (50, 37), 9, synth.STREAM_X, 1.0, mu=mu)
+    np.testing.assert_array_equal(bits(t).ravel(), synth.normal_bf16(9, synth.STREAM_X, 0, 1850, 1.0, mu))
+
+
+def _check_layer_against_oracle(wl, L: GpuLayer):
+    y = L.forward()
+    assert rde.device_status(L.cfg, L.ws) == 0
+    it = L.intermediates()
+    x = bits(L.inp["x"])
+    w_r = L.inp["w_router"].cpu().numpy()
+    bias = None if L.inp["bias"] is None else L.inp["bias"].cpu().numpy()
+    experts = [L.expert_weights_host(e) for e in range(wl.E)]
+    shared = L.expert_weights_host("shared") if wl.has_shared else None
+    logits = it["logits"].cpu().numpy()
+
+    # step 1a: router GEMM against the fp64 oracle
+    lo = oracle.router_logits(x, w_r)
+    assert np.abs(logits - lo).max() <= 1e-5 * np.abs(lo).max() + 1e-6
+
+    # the whole layer on identical logits
+    ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, **route_kwargs(wl))
+    np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_allclose(it["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-6, atol=1e-7)
+    np.testing.assert_array_equal(it["counts"].cpu().numpy(), ref["counts"])
+    np.testing.assert_array_equal(it["offsets"].cpu().numpy(), ref["offsets"])
+    np.testing.assert_array_equal(it["inv_pos"].cpu().numpy(), ref["inv_pos"])
+    np.testing.assert_array_equal(it["row_token"].cpu().numpy(), ref["row_token"])
+    rw = it["row_weight"].cpu().numpy()
+    np.testing.assert_array_equal(rw[ref["inv_pos"].ravel()], it["topk_w"].cpu().numpy().ravel())
+    R = wl.T * wl.k
+    xd = bits(it["xd"])
+    np.testing.assert_array_equal(xd[:R], ref["xd"])
+    if wl.has_shared:
+        np.testing.assert_array_equal(xd[R:], x)
+
+    # expert outputs per row (route-weighted), and the shared expert's rows
+    yd = oracle.bf16_to_double(bits(it["yd"]))
+    o_w = ref["o_rows"] * rw[:, None].astype(np.float64)
+    err = np.abs(yd[:R] - o_w).max(axis=1) / np.maximum(np.abs(o_w).max(axis=1), 1e-30)
+    assert err.max() <= BF16_TOL, f"routed rows: max rel err {err.max()}"
+    if wl.has_shared:
+        s = ref["shared_out"]
+        err = np.abs(yd[R:] - s).max(axis=1) / np.maximum(np.abs(s).max(axis=1), 1e-30)
+        assert err.max() <= BF16_TOL, f"shared rows: max rel err {err.max()}"
+
+    # layer output, every token
+    e = rel_err_per_token(bits(y), ref["y"])
+    assert e.max() <= BF16_TOL, f"y: max rel err {e.max()} at token {e.argmax()}"
+
+    # routing on the oracle's own fp64 logits agrees wherever the decision is not a near-tie
+    idx2, _ = oracle.route(lo, bias, **route_kwargs(wl))
+    keep = selection_margin(wl, lo, bias) >= MARGIN
+    assert keep.mean() > 0.5
+    np.testing.assert_array_equal(np.sort(idx2[keep], axis=1), np.sort(ref["topk_idx"][keep], axis=1))
+    return ref
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_matches_oracle(name):
+    wl = SMALL[name]
+    L = GpuLayer(wl)
+    _check_layer_against_oracle(wl, L)
+
+
+def test_forward_is_deterministic():
+    wl = SMALL["dsv3_small"]
+    L = GpuLayer(wl)
+    y1 = L.forward().clone()
+    yd1 = L.intermediates()["yd"].clone()
+    y2 = L.forward()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(yd1.view(torch.int16), L.intermediates()["yd"].view(torch.int16))
+
+
+def test_steps_through_their_own_entry_points():
+    """moe_route (with and without given logits), moe_dispatch, moe_expert_ffn and moe_combine called
+    one by one give what moe_forward gives."""
+    wl = SMALL["dsv3_small"]
+    L = GpuLayer(wl)
+    y_fwd = L.forward().clone()
+    it = L.intermediates()
+    dev = "cuda"
+    T, k, E, h = wl.T, wl.k, wl.E, wl.h
+    R_tot = T * k + T
+    cfg = L.cfg
+    ws = rde.alloc_workspace(cfg)
+    rde.device_status(cfg, ws)
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    rde.route(cfg, L.inp["x"], L.weights, idx, w, logits=logits, ws=ws)
+    assert torch.equal(logits, it["logits"]) and torch.equal(idx, it["topk_idx"]) and torch.equal(w, it["topk_w"])
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(w)
+    rde.route(cfg, None, L.weights, idx2, w2, logits=logits, logits_given=True)
+    assert torch.equal(idx2, idx) and torch.equal(w2, w)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty(T, k, dtype=torch.int32, device=dev)
+    row_token = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_weight = torch.empty(T * k, dtype=torch.float32, device=dev)
+    xd = torch.empty(R_tot, h, dtype=torch.bfloat16, device=dev)
+    rde.dispatch(cfg, L.inp["x"], idx, w, counts, offsets, inv_pos, row_token, row_weight, xd, None, ws)
+    for a, b in ((counts, "counts"), (offsets, "offsets"), (inv_pos, "inv_pos"), (row_token, "row_token"),
+                 (row_weight, "row_weight")):
+        assert torch.equal(a, it[b]), b
+    assert torch.equal(xd.view(torch.int16), it["xd"].view(torch.int16))
+    yd = torch.empty(R_tot, h, dtype=torch.bfloat16, device=dev)
+    rde.expert_ffn(cfg, L.weights, xd, None, offsets, row_weight, yd, ws)
+    assert torch.equal(yd.view(torch.int16), it["yd"].view(torch.int16))
+    y = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+    rde.combine(cfg, yd, inv_pos, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_fwd.view(torch.int16))
+    assert rde.device_status(cfg, ws) == 0
+
+
+def test_combine_identity_experts_closed_form():
+    """With identity experts (yd = route weight x token row, shared row = the token row) combine
+    returns x * (sum of the token's weights + 1)."""
+    wl = SMALL["dsv3_small"]
+    L = GpuLayer(wl)
+    L.forward()
+    it = L.intermediates()
+    R = wl.T * wl.k
+    xd = it["xd"].float()
+    yd = torch.empty_like(it["yd"])
+    yd[:R] = (xd[:R] * it["row_weight"][:, None]).to(torch.bfloat16)
+    yd[R:] = it["xd"][R:]
+    y = torch.empty_like(L.inp["x"])
+    rde.combine(L.cfg, yd, it["inv_pos"], y)
+    torch.cuda.synchronize()
+    x = oracle.bf16_to_double(bits(L.inp["x"]))
+    wsum = it["topk_w"].double().sum(dim=1).cpu().numpy()
+    ref = x * (wsum[:, None] + 1.0)
+    e = rel_err_per_token(bits(y), ref)
+    assert e.max() <= 2 ** -7
+    assert abs(wsum.mean() - wl.routed_scale) < 1e-5  # renormalised weights sum to the scaling factor
+
+
+def test_zero_tokens_is_a_no_op():
+    wl = SMALL["dsv3_small"].replace(T=0)
+    cfg = cfg_of(wl)
+    L = GpuLayer(SMALL["dsv3_small"])
+    ws = rde.alloc_workspace(cfg)
+    y = torch.full((1, wl.h), 7.0, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((1, wl.h), dtype=torch.bfloat16, device="cuda")
+    rde.forward(cfg, x, L.weights, y, ws)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+def test_bad_expert_index_is_skipped_and_reported():
+    wl = SMALL["dsv3_small"]
+    L = GpuLayer(wl)
+    L.forward()
+    it = L.intermediates()
+    cfg = L.cfg
+    T, k, E = wl.T, wl.k, wl.E
+    idx = it["topk_idx"].clone()
+    idx[3, 0] = E
+    idx[10, 5] = -7
+    ws = rde.alloc_workspace(cfg)
+    assert rde.device_status(cfg, ws) in (0, 1, 2, 3)  # clear whatever the new workspace held
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    inv_pos = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    row_token = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    row_weight = torch.empty(T * k, dtype=torch.float32, device="cuda")
+    xd = torch.empty(T * k + T, wl.h, dtype=torch.bfloat16, device="cuda")
+    rde.dispatch(cfg, L.inp["x"], idx, it["topk_w"], counts, offsets, inv_pos, row_token, row_weight, xd, None, ws)
+    assert rde.device_status(cfg, ws) == rde.moe.MOE_STATUS_BAD_EXPERT_INDEX
+    ip = inv_pos.cpu().numpy()
+    assert ip[3, 0] == -1 and ip[10, 5] == -1
+    good = idx.cpu().numpy()
+    valid = (good >= 0) & (good < E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(good[valid], minlength=E))
+    rows = ip[valid]
+    assert sorted(rows.tolist()) == list(range(int(valid.sum())))
+
+
+def test_fp8_dispatch_is_bit_exact():
+    wl = SMALL["dsv3_small"].replace(dtype="fp8")
+    cfg = cfg_of(wl)
+    inp = synth.device_inputs(wl, torch, with_weights=False)
+    T, k, E, h = wl.T, wl.k, wl.E, wl.h
+    dev = "cuda"
+    ws = rde.alloc_workspace(cfg)
+    rde.device_status(cfg, ws)
+    w_only = rde.Weights(w_router=inp["w_router"], bias=inp["bias"])
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    rde.route(cfg, inp["x"], w_only, idx, w, ws=ws)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty(T, k, dtype=torch.int32, device=dev)
+    row_token = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_weight = torch.empty(T * k, dtype=torch.float32, device=dev)
+    xd = torch.empty(T * k + T, h, dtype=torch.uint8, device=dev)
+    xs = torch.empty(T * k + T, h // 128, dtype=torch.float32, device=dev)
+    rde.dispatch(cfg, inp["x"], idx, w, counts, offsets, inv_pos, row_token, row_weight, xd, xs, ws)
+    torch.cuda.synchronize()
+    xq, xsc = oracle.quant_1x128(oracle.bf16_to_double(bits(inp["x"])))
+    rt = row_token.cpu().numpy()
+    np.testing.assert_array_equal(xd[:T * k].cpu().numpy(), xq[rt])
+    np.testing.assert_array_equal(xs[:T * k].cpu().numpy(), xsc[rt])
+    np.testing.assert_array_equal(xd[T * k:].cpu().numpy(), xq)
+    np.testing.assert_array_equal(xs[T * k:].cpu().numpy(), xsc)
+
+
+def test_fp8_weight_quantiser_is_bit_exact():
+    g = torch.Generator(device="cpu").manual_seed(3)
+    w = (torch.randn(3, 256, 384, generator=g) * 0.02)
+    w[1, :128, :128] = 0.0  # an all-zero tile -> scale 1
+    w[2, 5, 7] = 30.0  # an outlier in one tile
+    wb = w.to(torch.bfloat16).cuda()
+    q, s = rde.quantize_weights_fp8(wb)
+    torch.cuda.synchronize()
+    wbits = bits(wb)
+    for b in range(3):
+        rq, rs = oracle.quant_weight_128x128(wbits[b])
+        np.testing.assert_array_equal(q[b].cpu().numpy(), rq)
+        np.testing.assert_array_equal(s[b].cpu().numpy(), rs)
+    assert s[1, 0, 0].item() == 1.0
