@@ -155,6 +155,27 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, 
                  int32_t* counts, int32_t* offsets, int32_t* inv_pos, int32_t* row_token, float* row_weight,
                  void* xd, float* xd_scales, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Dispatch for callers that cannot allocate device memory. No counterpart on the pages: it is
+ * moe_dispatch (same arguments and outputs, same kernels) minus the workspace, for callers that
+ * cannot give the library a workspace -- an engine whose memory pool owns all of device memory and
+ * allows no other allocation, or a plug-in hook that only sees the layer's inputs and outputs
+ * (cudaMalloc may also synchronise the whole device, which such callers cannot afford).
+ * Its scratch (per-block histograms, 512 KiB) is a static array in the library's own device memory,
+ * held by every GPU that loads the library until the process exits. Limits and behaviour:
+ *   - ceil(T / 512) * E must not exceed 131072 (e.g. E = 256 allows T up to 262144); larger sizes
+ *     return MOE_ERR_UNSUPPORTED before any work is enqueued;
+ *   - allocates nothing: no cudaMalloc / cudaFree / allocating library routine;
+ *   - the first call on a device looks up the array's device address on that device (set-up), so
+ *     make that first call before any stream capture;
+ *   - every call shares the one array, so calls that overlap on the GPU (other streams, other host
+ *     threads) race and must be serialised by the caller;
+ *   - a topk_idx entry outside [0, E) is skipped (inv_pos = -1) as in moe_dispatch, but the status
+ *     bit is not reported (there is no workspace to hold it).
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+int moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_w,
+                         int32_t* counts, int32_t* offsets, int32_t* inv_pos, int32_t* row_token, float* row_weight,
+                         void* xd, float* xd_scales, moe_stream_t stream);
+
 /* Step 3, the experts (guide 6.4 section 2.1: gate, up, down; Perplexity "Roofline / GroupGEMM":
  * g groups of [m_i, k] x [k, n]; Perplexity "Quantization": SiLU, FP8 block scales). One grouped
  * GEMM per projection over the E routed experts plus the shared expert, tiled on the tensor cores:

@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -393,5 +394,100 @@ MOE_EXPORT int moe_device_status(const moe_config* cfg, void* ws, int32_t* statu
   if (e != cudaSuccess) return cuda_fail(e, "status read-back");
   *status = v;
   if (v) return fail(MOE_ERR_DEVICE, "device status bits set: " + std::to_string(v));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// Dispatch without a workspace.
+//
+// For callers that cannot give the library any device memory of their own: an engine that has
+// handed all of device memory to its own pool and permits no other allocation, or a plug-in hook
+// whose interface passes only the layer's inputs and outputs (cudaMalloc can also synchronise the
+// whole device, which such callers must not do). The dispatch step then takes its scratch (the
+// per-block expert histograms and the status word) from an array that lives in the library's own
+// global memory. Every GPU that loads the library holds this array until the process exits.
+// ------------------------------------------------------------------------------------------
+constexpr size_t kNoAllocHistInts = 131072;  // 512 KiB of histograms: ceil(T / 512) * E entries at most
+constexpr size_t kNoAllocStatusInts = 64;    // status word, padded to keep the histograms 256-byte aligned
+
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocStatusInts + kNoAllocHistInts];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device. The name is only a host-side stand-in;
+// the address is looked up once per device, with that device current, on the first call there.
+int noalloc_scratch(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device ordinal beyond 63");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static dispatch scratch");
+    g_noalloc_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+MOE_EXPORT int moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                    const float* topk_w, int32_t* counts, int32_t* offsets, int32_t* inv_pos,
+                                    int32_t* row_token, float* row_weight, void* xd, float* xd_scales,
+                                    moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  const size_t need = moe::dispatch_scratch_ints(cfg->T, cfg->E);
+  if (need > kNoAllocHistInts)
+    return fail(MOE_ERR_UNSUPPORTED, "moe_dispatch_noalloc: ceil(T / 512) * E = " + std::to_string(need) +
+                                         " histogram entries exceed the static scratch of " +
+                                         std::to_string(kNoAllocHistInts) + "; use moe_dispatch with a workspace");
+  REQUIRE_PTR(x, "x");
+  REQUIRE_PTR(topk_idx, "topk_idx");
+  REQUIRE_PTR(topk_w, "topk_w");
+  REQUIRE_PTR(counts, "counts");
+  REQUIRE_PTR(offsets, "offsets");
+  REQUIRE_PTR(inv_pos, "inv_pos");
+  REQUIRE_PTR(row_token, "row_token");
+  REQUIRE_PTR(row_weight, "row_weight");
+  REQUIRE_PTR(xd, "xd");
+  if (cfg->dtype == MOE_DTYPE_FP8_BLOCK128) REQUIRE_PTR(xd_scales, "xd_scales");
+  int32_t* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the status word accumulates bits with atomicOr: it must start at zero; the histograms are written
+  // in full before they are read, so they need no clearing
+  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static dispatch status word");
+  moe::DispatchDesc d;
+  d.x = x;
+  d.topk_idx = topk_idx;
+  d.topk_w = topk_w;
+  d.counts = counts;
+  d.offsets = offsets;
+  d.inv_pos = inv_pos;
+  d.row_token = row_token;
+  d.row_weight = row_weight;
+  d.xd = xd;
+  d.xd_scales = xd_scales;
+  d.scratch = scratch + kNoAllocStatusInts;
+  d.status = scratch;
+  d.T = cfg->T;
+  d.h = cfg->h;
+  d.E = cfg->E;
+  d.k = cfg->k;
+  d.shared = cfg->I_shared > 0;
+  d.fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+  e = moe::launch_dispatch(d, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  if (cfg->T > 0) counted(4);
   return MOE_OK;
 }

@@ -66,6 +66,7 @@ def load():
                 "moe_workspace_layout": [cfgp, ctypes.POINTER(MoeWsLayout)],
                 "moe_route": [cfgp, vp, wp, vp, i32, vp, vp, vp, sz, vp],
                 "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                "moe_dispatch_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
                 "moe_expert_ffn": [cfgp, wp, vp, vp, vp, vp, vp, vp, sz, vp],
                 "moe_combine": [cfgp, vp, vp, vp, vp],
                 "moe_forward": [cfgp, vp, wp, vp, vp, sz, vp],
@@ -152,6 +153,14 @@ def dispatch(cfg, x, topk_idx, topk_w, counts, offsets, inv_pos, row_token, row_
     _check(load().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(offsets),
                                _ptr(inv_pos), _ptr(row_token), _ptr(row_weight), _ptr(xd), _ptr(xd_scales), _ptr(ws),
                                ws.numel(), _stream()))
+
+
+def dispatch_noalloc(cfg, x, topk_idx, topk_w, counts, offsets, inv_pos, row_token, row_weight, xd, xd_scales):
+    """moe_dispatch without a workspace, for callers that cannot allocate device memory (scratch is a
+    static array inside the library; concurrent calls race; see include/moe.h)."""
+    _check(load().moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                       _ptr(offsets), _ptr(inv_pos), _ptr(row_token), _ptr(row_weight), _ptr(xd),
+                                       _ptr(xd_scales), _stream()))
 
 
 def expert_ffn(cfg, weights: Weights, xd, xd_scales, offsets, row_weight, yd, ws):
