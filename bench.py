@@ -224,6 +224,8 @@ def main():
     ap.add_argument("--workload", default="dsv3_prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None, help="override T (small profiling cases)")
+    ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -231,6 +233,9 @@ def main():
     import synth
 
     wl = synth.WORKLOADS[args.workload]
+    if args.tokens is not None or args.experts is not None:
+        wl = wl.replace(name=f"{wl.name}_T{args.tokens or wl.T}_E{args.experts or wl.E}", T=args.tokens or wl.T,
+                        E=args.experts or wl.E)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

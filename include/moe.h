@@ -109,6 +109,7 @@ typedef struct {
   size_t hbuf;       /* [R_tot, I] bf16 or e4m3 (SwiGLU product) */
   size_t h_scales;   /* FP8: [R_tot, I/128] fp32 */
   size_t yd;         /* [R_tot, h] bf16 expert outputs (routed rows already route-weighted) */
+  size_t router_w3;  /* [3, E, h] bf16: the router weight as three bf16 terms (tensor-core router) */
   size_t scratch;    /* per-call scratch (histograms, status word) */
   size_t total;      /* bytes required */
 } moe_ws_layout;
@@ -119,17 +120,20 @@ int moe_workspace_size(const moe_config* cfg, size_t* bytes);
 int moe_workspace_layout(const moe_config* cfg, moe_ws_layout* layout);
 
 /* Step 1, routing (Ultralytics "How tokens move across GPUs", step 1; TensorRT-LLM "DeepSeek R1
- * throughput on Blackwell", "Top-K kernel fusion": groups first, then the top experts inside
- * them, with a bias and a scaling factor; Perplexity "MoE Router": Mixtral routing is the case
- * top-k-group = all groups; the bias only selects, Ultralytics "Load balancing and capacity").
+ * throughput on Blackwell", "RouterGEMM mixed I/O" (bf16 in, fp32 out) and "Top-K kernel fusion":
+ * groups first, then the top experts inside them, with a bias and a scaling factor; Perplexity "MoE
+ * Router": Mixtral routing is the case top-k-group = all groups; the bias only selects, Ultralytics
+ * "Load balancing and capacity").
  *   x        [T, h] bf16 activations (unused with MOE_LOGITS_GIVEN)
  *   weights  w_router and bias are read
- *   logits   [T, E] fp32: output of the router GEMM (fp32 accumulation), or the input when
- *            flags & MOE_LOGITS_GIVEN; may be NULL without the flag (then kept in ws)
+ *   logits   [T, E] fp32: output of the router GEMM (fp32-accurate: on the tensor cores with the
+ *            weight split into three bf16 terms when E >= 128 and E % 32 == 0, on the CUDA cores in
+ *            fp32 otherwise), or the input when flags & MOE_LOGITS_GIVEN; may be NULL without the
+ *            flag (then kept in ws)
  *   topk_idx [T, k] int32 out: chosen experts, descending selection key, ties to lower index
  *   topk_w   [T, k] fp32 out: route weights (softmax probability or sigmoid score,
  *            renormalised if asked, times routed_scale)
- *   ws       workspace of moe_workspace_size() bytes (ws_bytes), or NULL if logits != NULL
+ *   ws       workspace of moe_workspace_size() bytes (ws_bytes); may be NULL with MOE_LOGITS_GIVEN
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA. */
 int moe_route(const moe_config* cfg, const void* x, const moe_weights* weights, float* logits, int flags,
               int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);

@@ -84,6 +84,7 @@ Layout make_layout(const moe_config* c) {
   l.hbuf = take((fp8 ? 1 : 2) * L.R_tot * I);
   l.h_scales = take(fp8 ? sizeof(float) * L.R_tot * (I / 128) : 0);
   l.yd = take(2 * L.R_tot * h);
+  l.router_w3 = take(2 * 3 * E * h);
   l.scratch = take(256 + sizeof(int32_t) * moe::dispatch_scratch_ints(c->T, c->E));
   l.total = o;
   return L;
@@ -116,13 +117,44 @@ int check_ws(void* ws, size_t ws_bytes, const Layout& L) {
     if (!aligned16(p)) return fail(MOE_ERR_INVALID, std::string(name) + " must be 16-byte aligned"); \
   } while (0)
 
+bool tensor_core_router(const moe_config* c) { return c->E >= 128 && c->E % 32 == 0; }
+
 int do_route(const moe_config* c, const void* x, const moe_weights* w, float* logits, int flags, int32_t* topk_idx,
-             float* topk_w, cudaStream_t stream) {
+             float* topk_w, void* ws, const Layout& L, cudaStream_t stream) {
   cudaError_t e;
-  if (!(flags & MOE_LOGITS_GIVEN)) {
-    e = moe::launch_router_gemm(x, w->w_router, logits, c->T, c->h, c->E, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
-    if (c->T > 0) counted(1);
+  if (!(flags & MOE_LOGITS_GIVEN) && c->T > 0) {
+    if (tensor_core_router(c)) {
+      void* w3 = at<void>(ws, L.l.router_w3);
+      e = moe::launch_split_router_weight(w->w_router, w3, (int64_t)c->E * c->h, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "router weight split launch");
+      std::string err;
+      moe::GroupedGemmDesc g;
+      g.A = x;
+      g.a_rows = c->T;
+      g.B = w3;
+      g.Bs = nullptr;
+      g.b_rows = c->E;
+      g.offsets = nullptr;
+      g.E = 1;
+      g.R = 0;
+      g.T = c->T;
+      g.K = c->h;
+      g.N = c->E;
+      g.I = 0;
+      g.mode = 2;
+      g.ksplit = 3;
+      g.out = logits;
+      g.ldo = c->E;
+      g.row_weight = nullptr;
+      g.status = status_ptr(ws, L.l);
+      e = moe::launch_grouped_gemm_bf16(g, stream, &err);
+      if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "router GEMM launch") : cuda_fail(e, err.c_str());
+      counted(2);
+    } else {
+      e = moe::launch_router_gemm(x, w->w_router, logits, c->T, c->h, c->E, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
+      counted(1);
+    }
   }
   moe::TopkDesc d;
   d.logits = logits;
@@ -269,18 +301,17 @@ MOE_EXPORT int moe_route(const moe_config* cfg, const void* x, const moe_weights
     REQUIRE_PTR(x, "x");
     if (!weights) return fail(MOE_ERR_INVALID, "weights is NULL");
     REQUIRE_PTR(weights->w_router, "weights->w_router");
-    if (!logits) {
-      if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+    if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+    if (!logits)
       logits = at<float>(ws, L.l.logits);
-    } else if (!aligned16(logits)) {
+    else if (!aligned16(logits))
       return fail(MOE_ERR_INVALID, "logits must be 16-byte aligned");
-    }
   }
   if (cfg->score == MOE_SCORE_SIGMOID && weights && weights->bias && !aligned16(weights->bias))
     return fail(MOE_ERR_INVALID, "weights->bias must be 16-byte aligned");
   REQUIRE_PTR(topk_idx, "topk_idx");
   REQUIRE_PTR(topk_w, "topk_w");
-  return do_route(cfg, x, weights, logits, flags, topk_idx, topk_w, (cudaStream_t)stream);
+  return do_route(cfg, x, weights, logits, flags, topk_idx, topk_w, ws, L, (cudaStream_t)stream);
 }
 
 MOE_EXPORT int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_w,
@@ -351,7 +382,7 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
   const moe_ws_layout& l = L.l;
   if ((rc = do_route(cfg, x, weights, at<float>(ws, l.logits), 0, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w),
-                     s)))
+                     ws, L, s)))
     return rc;
   if ((rc = do_dispatch(cfg, x, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w), at<int32_t>(ws, l.counts),
                         at<int32_t>(ws, l.offsets), at<int32_t>(ws, l.inv_pos), at<int32_t>(ws, l.row_token),

@@ -7,6 +7,11 @@
 // section 2.1: gate, up, down) are two launches:
 //   mode 0  H  = silu(A W_gate^T) * (A W_up^T)     A = xd [R_tot, h], W_gu [E, 2I, h]
 //   mode 1  yd = (A W_down^T) * row_weight         A = H  [R_tot, I], W_d  [E, h, I]
+// and the router GEMM of the same layer as a single group (TensorRT-LLM "DeepSeek R1 throughput on
+// Blackwell", "RouterGEMM mixed I/O": bf16 activations in, fp32 logits out):
+//   mode 2  logits = x (W_hi + W_mid + W_lo)^T     A = x [T, h], B = the fp32 router weight split into
+//           three bf16 terms [3, E, h]; x is exact in bf16 and every bf16 x bf16 product is exact in
+//           fp32, so the three K passes accumulate an fp32-accurate x W^T on the tensor cores.
 // Work follows the device-side per-expert counts (Perplexity, "Quantization": kernels read the
 // routing information to split the work, instead of sizing it from buffer bounds), so the launch
 // needs no host read-back and has a fixed grid.
@@ -55,8 +60,10 @@ struct Args {
   int T;
   int K;        // reduction length (multiple of BK)
   int n_tiles;  // output column tiles per group
-  int mode;     // 0: gate/up + SwiGLU -> H; 1: down * row_weight -> yd
+  int mode;     // 0: gate/up + SwiGLU -> H; 1: down * row_weight -> yd; 2: router, fp32 out
   int I;        // mode 0: row offset of the up half inside W_gu
+  int ksplit;   // B is split into ksplit K passes over the same A (mode 2: 3), else 1
+  int n_valid;  // mode 2: output columns that exist (E)
   int ldo;      // output row stride in elements
   void* out;
   const float* row_weight;
@@ -135,7 +142,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       int g = base + lane;
       int row0 = 0, m = 0;
       if (g < G) {
-        if (g < args.E) {
+        if (args.offsets == nullptr) {  // one group: rows [0, T)
+          row0 = 0;
+          m = args.T;
+        } else if (g < args.E) {
           row0 = args.offsets[g];
           m = args.offsets[g + 1] - row0;
         } else {
@@ -158,7 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       s.gtile[G] = carry;
-      s.grow[G] = args.shared ? args.R + args.T : args.offsets[args.E];
+      s.grow[G] = args.offsets == nullptr ? args.T : (args.shared ? args.R + args.T : args.offsets[args.E]);
       for (int i = 0; i < STAGES; ++i) {
         mbar_init(&s.full[i], 1);
         mbar_init(&s.empty[i], 1);
@@ -184,7 +194,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_slot;
   const int total = s.gtile[G] * args.n_tiles;
-  const int kblocks = args.K / BK;
+  const int kpb = args.K / BK;  // K blocks per pass over A
+  const int kblocks = kpb * args.ksplit;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       Tile t = decode(s, G, args.n_tiles, tile);
       const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
-      int z = t.g < args.E ? t.g : 0;
+      const int zg = t.g < args.E ? t.g : 0;
       int n0, n1;
       if (args.mode == 0) {
         n0 = t.n_tile * (BN / 2);
@@ -211,10 +222,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint8_t* a = smem + stage * STAGE_BYTES;
         uint8_t* b = a + A_BYTES;
+        const int pass = kb / kpb;
+        const int ka = (kb - pass * kpb) * BK;
+        const int z = args.ksplit > 1 ? pass : zg;
         mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
-        tma_load_2d(a, &tmA, &s.full[stage], kb * BK, t.a_row);
-        tma_load_3d(b, mb, &s.full[stage], kb * BK, n0, z);
-        tma_load_3d(b + B_BYTES / 2, mb, &s.full[stage], kb * BK, n1, z);
+        tma_load_2d(a, &tmA, &s.full[stage], ka, t.a_row);
+        tma_load_3d(b, mb, &s.full[stage], ka, n0, z);
+        tma_load_3d(b + B_BYTES / 2, mb, &s.full[stage], ka, n1, z);
         ++issued;
         if (++stage == STAGES) {
           stage = 0;
@@ -307,6 +321,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          }
+        }
+      } else if (args.mode == 2) {
+        float* out = reinterpret_cast<float*>(args.out) + orow * args.ldo + t.n_tile * BN;
+        const int ncols = min(BN, args.n_valid - t.n_tile * BN);  // a multiple of 32
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (valid && c < ncols) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
       } else {
@@ -421,8 +449,9 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   }
   CUtensorMap tA, tB, tBs;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int ksplit = d.ksplit > 1 ? d.ksplit : 1;
   bool ok = encode_2d(&tA, d.A, BF, 2, d.a_rows, d.K, gg::BM) &&
-            encode_3d(&tB, d.B, BF, 2, d.E, d.b_rows, d.K, gg::BN / 2) &&
+            encode_3d(&tB, d.B, BF, 2, ksplit > 1 ? ksplit : d.E, d.b_rows, d.K, gg::BN / 2) &&
             encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, gg::BN / 2);
   if (!ok) {
     *err = "cuTensorMapEncodeTiled rejected a grouped-GEMM operand";
@@ -437,7 +466,9 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.K = d.K;
   a.mode = d.mode;
   a.I = d.I;
-  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : d.N / gg::BN;
+  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, gg::BN);
+  a.ksplit = ksplit;
+  a.n_valid = d.N;
   a.ldo = d.ldo;
   a.out = d.out;
   a.row_weight = d.row_weight;

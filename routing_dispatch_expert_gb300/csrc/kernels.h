@@ -14,6 +14,10 @@ int num_sms();
 cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, int T, int h, int E,
                                cudaStream_t stream);
 
+// Step 1: the fp32 router weight as three bf16 terms hi + mid + lo (w3 [3, E, h]) for the tensor-core
+// router GEMM (grouped GEMM mode 2).
+cudaError_t launch_split_router_weight(const float* w, void* w3, int64_t n, cudaStream_t stream);
+
 // Step 1: top-k selection and route weights from fp32 logits, one warp per token.
 struct TopkDesc {
   const float* logits;
@@ -54,9 +58,10 @@ struct GroupedGemmDesc {
   const void* B;   // [E, b_rows, K]
   const void* Bs;  // [b_rows, K] shared expert or nullptr
   int64_t b_rows;
-  const int32_t* offsets;
+  const int32_t* offsets;  // nullptr: a single group of rows [0, T) (router)
   int E, R, T, K, N, I;
-  int mode;  // 0 gate/up -> H, 1 down -> yd
+  int mode;  // 0 gate/up -> H, 1 down -> yd, 2 router logits (fp32)
+  int ksplit = 1;  // mode 2: B holds 3 bf16 terms of the fp32 weight, [3, N, K]
   void* out;
   int ldo;
   const float* row_weight;

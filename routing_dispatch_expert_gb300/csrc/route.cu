@@ -128,6 +128,32 @@ cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, i
 }
 
 // ------------------------------------------------------------------------------------------
+// The fp32 router weight as three bf16 terms for the tensor-core router GEMM: hi = bf16(w),
+// mid = bf16(w - hi), lo = bf16(w - hi - mid). Each difference is exact in fp32, so hi + mid + lo
+// carries 24 significant bits of w (the fp32 significand).
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) split_router_weight_kernel(const float* __restrict__ w,
+                                                                  __nv_bfloat16* __restrict__ w3, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = __fsub_rn(v, __bfloat162float(hi));
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = __fsub_rn(r1, __bfloat162float(mid));
+    w3[i] = hi;
+    w3[n + i] = mid;
+    w3[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+cudaError_t launch_split_router_weight(const float* w, void* w3, int64_t n, cudaStream_t stream) {
+  int64_t blocks = cdiv(n, 256);
+  if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
+  split_router_weight_kernel<<<(unsigned)blocks, 256, 0, stream>>>(w, reinterpret_cast<__nv_bfloat16*>(w3), n);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
 // top-k: one warp per token; lane l holds experts [l * EPL, l * EPL + EPL).
 // ------------------------------------------------------------------------------------------
 namespace tk {

@@ -43,7 +43,7 @@ class MoeWeightsStruct(ctypes.Structure):
 class MoeWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "inv_pos",
                                                "row_token", "row_weight", "xd", "xd_scales", "hbuf", "h_scales", "yd",
-                                               "scratch", "total")]
+                                               "router_w3", "scratch", "total")]
 
 
 _lock = threading.Lock()

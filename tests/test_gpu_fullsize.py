@@ -106,7 +106,7 @@ def test_full_size_fp8_routing_and_dispatch():
     np.testing.assert_array_equal(offsets.cpu().numpy(), off)
     np.testing.assert_array_equal(inv_pos.cpu().numpy(), ip)
     # Zipf(1.0) skew: the hottest expert takes far more than the mean
-    assert c.max() > 8 * c.mean()
+    assert c.max() > 4 * c.mean()
     rows = _sample(T * k, 256, 4)
     x = bits(inp["x"])
     xq, xsc = oracle.quant_1x128(oracle.bf16_to_double(x[rt[rows]]))

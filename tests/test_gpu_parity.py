@@ -23,6 +23,9 @@ SMALL = {
     "dsv3_skew": _W["dsv3_decode"].replace(name="dsv3_skew", T=77, h=512, E=64, I=256, I_shared=256),
     "dsv3_hot": _W["dsv3_decode"].replace(name="dsv3_hot", T=400, h=256, E=64, I=128, I_shared=128, zipf_s=6.0),
     "single_token": _W["dsv3_prefill"].replace(name="single_token", T=1, h=256, E=64, I=128, I_shared=128),
+    # E >= 128: the router GEMM runs on the tensor cores (fp32 weight as three bf16 terms)
+    "dsv3_e256": _W["dsv3_prefill"].replace(name="dsv3_e256", T=300, h=512, E=256, I=128, I_shared=128),
+    "dsv3_e128_skew": _W["dsv3_decode"].replace(name="dsv3_e128_skew", T=130, h=256, E=128, I=128, I_shared=128),
 }
 
 
@@ -41,7 +44,7 @@ def test_device_generator_matches_host_generator():
     np.testing.assert_array_equal(bits(t).ravel(), synth.normal_bf16(9, synth.STREAM_X, 0, 1850, 1.0, mu))
 
 
-def _check_layer_against_oracle(wl, L: GpuLayer):
+def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
     y = L.forward()
     assert rde.device_status(L.cfg, L.ws) == 0
     it = L.intermediates()
@@ -89,7 +92,7 @@ def _check_layer_against_oracle(wl, L: GpuLayer):
     # routing on the oracle's own fp64 logits agrees wherever the decision is not a near-tie
     idx2, _ = oracle.route(lo, bias, **route_kwargs(wl))
     keep = selection_margin(wl, lo, bias) >= MARGIN
-    assert keep.mean() > 0.5
+    assert keep.mean() >= min_clear
     np.testing.assert_array_equal(np.sort(idx2[keep], axis=1), np.sort(ref["topk_idx"][keep], axis=1))
     return ref
 
@@ -98,7 +101,9 @@ def _check_layer_against_oracle(wl, L: GpuLayer):
 def test_forward_matches_oracle(name):
     wl = SMALL[name]
     L = GpuLayer(wl)
-    _check_layer_against_oracle(wl, L)
+    # with Zipf(6) nearly every sigmoid saturates, the group scores no longer depend on the token and
+    # every token can sit on the same group-level near-tie: no share of clear tokens is required there
+    _check_layer_against_oracle(wl, L, min_clear=0.0 if name == "dsv3_hot" else 0.5)
 
 
 def test_forward_is_deterministic():
@@ -200,7 +205,7 @@ def test_bad_expert_index_is_skipped_and_reported():
     idx[3, 0] = E
     idx[10, 5] = -7
     ws = rde.alloc_workspace(cfg)
-    assert rde.device_status(cfg, ws) in (0, 1, 2, 3)  # clear whatever the new workspace held
+    rde.device_status(cfg, ws)  # a new workspace holds arbitrary bits: read and clear them first
     counts = torch.empty(E, dtype=torch.int32, device="cuda")
     offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     inv_pos = torch.empty(T, k, dtype=torch.int32, device="cuda")
