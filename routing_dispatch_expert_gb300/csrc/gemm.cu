@@ -11,7 +11,9 @@
 // Blackwell", "RouterGEMM mixed I/O": bf16 activations in, fp32 logits out):
 //   mode 2  logits = x (W_hi + W_mid + W_lo)^T     A = x [T, h], B = the fp32 router weight split into
 //           three bf16 terms [3, E, h]; x is exact in bf16 and every bf16 x bf16 product is exact in
-//           fp32, so the three K passes accumulate an fp32-accurate x W^T on the tensor cores.
+//           fp32. The tensor core's accumulator does not round like an IEEE fp32 add over thousands
+//           of steps, so the MMAs accumulate chunks of ROUTER_CHUNK K blocks in TMEM (double
+//           buffered, 128-column tiles) and the epilogue sums the chunks in fp32 registers.
 // Work follows the device-side per-expert counts (Perplexity, "Quantization": kernels read the
 // routing information to split the work, instead of sizing it from buffer bounds), so the launch
 // needs no host read-back and has a fixed grid.
@@ -51,6 +53,7 @@ constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = 1025;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int ROUTER_CHUNK = 8;  // K blocks (512 K elements) per TMEM partial sum in mode 2
 
 struct Args {
   const int32_t* offsets;  // [E + 1]
@@ -211,6 +214,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (args.mode == 0) {
         n0 = t.n_tile * (BN / 2);
         n1 = args.I + t.n_tile * (BN / 2);
+      } else if (args.mode == 2) {
+        n0 = t.n_tile * (BN / 2);  // 128-wide tiles: one B box
+        n1 = -1;
       } else {
         n0 = t.n_tile * BN;
         n1 = n0 + BN / 2;
@@ -225,10 +231,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pass = kb / kpb;
         const int ka = (kb - pass * kpb) * BK;
         const int z = args.ksplit > 1 ? pass : zg;
-        mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
+        mbar_arrive_expect_tx(&s.full[stage], n1 >= 0 ? STAGE_BYTES : A_BYTES + B_BYTES / 2);
         tma_load_2d(a, &tmA, &s.full[stage], ka, t.a_row);
         tma_load_3d(b, mb, &s.full[stage], ka, n0, z);
-        tma_load_3d(b + B_BYTES / 2, mb, &s.full[stage], ka, n1, z);
+        if (n1 >= 0) tma_load_3d(b + B_BYTES / 2, mb, &s.full[stage], ka, n1, z);
         ++issued;
         if (++stage == STAGES) {
           stage = 0;
@@ -247,17 +253,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+    // The accumulator holds one chunk of K blocks: the whole tile (modes 0, 1) or ROUTER_CHUNK
+    // blocks (mode 2, whose epilogue adds the chunks in fp32).
+    const uint32_t idesc = args.mode == 2 ? idesc_bf16(BM, BN / 2) : idesc_bf16(BM, BN);
+    const int ch_len = args.mode == 2 ? ROUTER_CHUNK : kblocks;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      if (!wait_or_abort(s, &s.tempty[acc], acc_phase ^ 1, args)) break;
-      tc_fence_after();
-      const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+      uint32_t d = 0;
       for (int kb = 0; kb < kblocks; ++kb) {
+        const int kc = kb % ch_len;
+        if (kc == 0) {
+          if (!wait_or_abort(s, &s.tempty[acc], acc_phase ^ 1, args)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          d = tmem_base + (uint32_t)(acc * BN);
+        }
         if (!wait_or_abort(s, &s.full[stage], phase, args)) {
           ok = false;
           break;
@@ -267,17 +283,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t b = a + A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          umma_f16(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), IDESC, (kb | kk) != 0);
+          umma_f16(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), idesc, (kc | kk) != 0);
         umma_commit(&s.empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
+        if (kc == ch_len - 1 || kb == kblocks - 1) {
+          umma_commit(&s.tfull[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
       }
-      if (!ok) break;
-      umma_commit(&s.tfull[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
     }
     // all MMAs issued by this thread complete before TMEM / shared memory go away
     umma_commit(&s.mma_done);
@@ -292,6 +309,53 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       Tile t = decode(s, G, args.n_tiles, tile);
+      if (args.mode == 2) {
+        // router: sum the TMEM chunk partials of this tile in fp32 registers, then store
+        float run[BN / 2];
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) run[i] = 0.f;
+        const int nch = (kblocks + ROUTER_CHUNK - 1) / ROUTER_CHUNK;
+        bool fine = true;
+        for (int ch = 0; ch < nch; ++ch) {
+          int ok = 1;
+          if (lane == 0) ok = wait_or_abort(s, &s.tfull[acc], acc_phase, args);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            fine = false;
+            break;
+          }
+          __syncwarp();
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll
+          for (int c = 0; c < BN / 2; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) run[c + i] = __fadd_rn(run[c + i], __uint_as_float(v[i]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.tempty[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
+        if (!fine) break;
+        const int ncols = min(BN / 2, args.n_valid - t.n_tile * (BN / 2));  // a multiple of 32
+        if (r < t.rows) {
+          float* out = reinterpret_cast<float*>(args.out) + ((int64_t)t.a_row + r) * args.ldo + t.n_tile * (BN / 2);
+#pragma unroll
+          for (int c = 0; c < BN / 2; c += 32)
+            if (c < ncols) {
+              float4* dst = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(run[c + 4 * i], run[c + 4 * i + 1], run[c + 4 * i + 2], run[c + 4 * i + 3]);
+            }
+        }
+        continue;
+      }
       // one lane waits, the warp follows: the tcgen05.ld below is warp-collective
       int ok = 1;
       if (lane == 0) ok = wait_or_abort(s, &s.tfull[acc], acc_phase, args);
@@ -321,20 +385,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-          }
-        }
-      } else if (args.mode == 2) {
-        float* out = reinterpret_cast<float*>(args.out) + orow * args.ldo + t.n_tile * BN;
-        const int ncols = min(BN, args.n_valid - t.n_tile * BN);  // a multiple of 32
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c, v);
-          tmem_ld_wait();
-          if (valid && c < ncols) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
       } else {
@@ -466,7 +516,7 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.K = d.K;
   a.mode = d.mode;
   a.I = d.I;
-  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, gg::BN);
+  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, d.mode == 2 ? gg::BN / 2 : gg::BN);
   a.ksplit = ksplit;
   a.n_valid = d.N;
   a.ldo = d.ldo;
