@@ -377,8 +377,15 @@ def main():
     flops, gemm_flops, bytes_ = layer_counts(wl, active)
     p_tc = peaks["bf16_tflops"] * 1e12
     p_hbm = peaks["hbm_gbs"] * 1e9
-    t_roof = max(flops / p_tc, bytes_ / p_hbm)
+    # the expert GEMMs run at their own dtype's peak: FP8 = the measured bf16 peak x the nominal
+    # dense ratio 4.5 / 2.25 PFLOP/s; the router stays bf16 (fp32-accurate split)
+    ratio = 2.0 if wl.dtype == "fp8" else 1.0
+    p_gemm = p_tc * ratio
+    t_compute = (flops - gemm_flops) / p_tc + gemm_flops / p_gemm
+    t_roof = max(t_compute, bytes_ / p_hbm)
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    gemm_peak = peaks["bf16_tflops"] * ratio
+    gemm_peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
     traffic = gemm_traffic_from_profile(wl)
 
     cpu = None
@@ -392,16 +399,18 @@ def main():
         line = {
             "metric": METRIC, "value": world * wl.T / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_of(wl, world),
-            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": gemm_tflops / peaks["bf16_tflops"], "traffic": traffic,
-                         "kernel": "grouped_gemm_bf16_kernel (gate/up + down launches of one step)",
-                         "peak_kind": f"bf16 burst, {peaks_kind}",
-                         "frac_of_sustained": gemm_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])},
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if wl.dtype == "fp8" else "bf16",
+            "data": "synthetic", "config": config_of(wl, world),
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": gemm_peak, "unit": "TFLOP/s",
+                         "frac": gemm_tflops / gemm_peak, "traffic": traffic,
+                         "kernel": ("grouped_gemm_fp8_kernel" if wl.dtype == "fp8" else "grouped_gemm_bf16_kernel")
+                                   + " (gate/up + down launches of one step)",
+                         "peak_kind": (f"fp8 = 2 x bf16 burst ({peaks_kind}), nominal ratio" if wl.dtype == "fp8"
+                                       else f"bf16 burst, {peaks_kind}"),
+                         "frac_of_sustained": gemm_tflops / gemm_peak_sus},
             "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3), "flops": flops,
                                "bytes": bytes_, "active_experts": active,
-                               "bound": "tensor" if flops / p_tc >= bytes_ / p_hbm else "hbm",
+                               "bound": "tensor" if t_compute >= bytes_ / p_hbm else "hbm",
                                "peaks": peaks_kind},
             "ms_moe_forward": ms_fwd, "ms_expert_ffn": gemm_ms,
             "e2e": {"value": world * wl.T / (ms_e2e * 1e-3), "unit": UNIT,

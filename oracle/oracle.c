@@ -135,6 +135,7 @@ static float orc_fp8_scale(double amax) {
  * run time per 128-element vector along K). v: [m, n] row-major doubles; n % 128 == 0.
  * q: [m, n] codes; s: [m, n/128] fp32 scales. */
 ORC_API void orc_quant_1x128(const double* v, int64_t m, int64_t n, uint8_t* q, float* s) {
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < m; ++r)
     for (int64_t b = 0; b < n / 128; ++b) {
       const double* blk = v + r * n + b * 128;
@@ -151,6 +152,7 @@ ORC_API void orc_quant_1x128(const double* v, int64_t m, int64_t n, uint8_t* q, 
  * tile). w: [rows, cols] bf16; rows % 128 == 0, cols % 128 == 0. q: [rows, cols] codes;
  * s: [rows/128, cols/128] fp32 scales. */
 ORC_API void orc_quant_weight_128x128(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* q, float* s) {
+#pragma omp parallel for schedule(static)
   for (int64_t br = 0; br < rows / 128; ++br)
     for (int64_t bc = 0; bc < cols / 128; ++bc) {
       double amax = 0.0;

@@ -207,11 +207,53 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
 int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, const float* xd_scales,
                   const int32_t* offsets, const float* row_weight, void* yd, void* ws, const Layout& L,
                   cudaStream_t stream) {
-  if (c->dtype == MOE_DTYPE_FP8_BLOCK128) return fail(MOE_ERR_UNSUPPORTED, "the FP8 expert GEMM is not built yet");
-  (void)xd_scales;
   if (c->T == 0) return MOE_OK;
   const bool shared = c->I_shared > 0;
   std::string err;
+  if (c->dtype == MOE_DTYPE_FP8_BLOCK128) {
+    moe::GroupedGemmFp8Desc g;
+    g.A = xd;
+    g.a_scales = xd_scales;
+    g.a_rows = L.R_tot;
+    g.B = w->w_gu;
+    g.b_scales = w->s_gu;
+    g.Bs = shared ? w->w_gu_shared : nullptr;
+    g.bs_scales = shared ? w->s_gu_shared : nullptr;
+    g.b_rows = 2 * (int64_t)c->I;
+    g.offsets = offsets;
+    g.E = c->E;
+    g.R = (int)L.R;
+    g.T = c->T;
+    g.K = c->h;
+    g.N = 2 * c->I;
+    g.I = c->I;
+    g.mode = 0;
+    g.out = at<void>(ws, L.l.hbuf);
+    g.out_scales = at<float>(ws, L.l.h_scales);
+    g.ldo = c->I;
+    g.row_weight = nullptr;
+    g.status = status_ptr(ws, L.l);
+    cudaError_t e = moe::launch_grouped_gemm_fp8(g, stream, &err);
+    if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "FP8 gate/up grouped GEMM launch") : cuda_fail(e, err.c_str());
+    g.A = at<void>(ws, L.l.hbuf);
+    g.a_scales = at<float>(ws, L.l.h_scales);
+    g.B = w->w_d;
+    g.b_scales = w->s_d;
+    g.Bs = shared ? w->w_d_shared : nullptr;
+    g.bs_scales = shared ? w->s_d_shared : nullptr;
+    g.b_rows = c->h;
+    g.K = c->I;
+    g.N = c->h;
+    g.mode = 1;
+    g.out = yd;
+    g.out_scales = nullptr;
+    g.ldo = c->h;
+    g.row_weight = row_weight;
+    e = moe::launch_grouped_gemm_fp8(g, stream, &err);
+    if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "FP8 down grouped GEMM launch") : cuda_fail(e, err.c_str());
+    counted(2);
+    return MOE_OK;
+  }
   moe::GroupedGemmDesc g;
   g.A = xd;
   g.a_rows = L.R_tot;
@@ -376,7 +418,6 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   if (!weights) return fail(MOE_ERR_INVALID, "weights is NULL");
   REQUIRE_PTR(weights->w_router, "weights->w_router");
   if ((rc = check_expert_weights(cfg, weights))) return rc;
-  if (cfg->dtype == MOE_DTYPE_FP8_BLOCK128) return fail(MOE_ERR_UNSUPPORTED, "the FP8 expert GEMM is not built yet");
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(status_ptr(ws, L.l), 0, sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "status reset");

@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -51,7 +52,6 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int MAX_GROUPS = 1025;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr int ROUTER_CHUNK = 8;  // K blocks (512 K elements) per TMEM partial sum in mode 2
 
@@ -82,51 +82,12 @@ struct Shared {
   uint64_t mma_done;
   uint32_t tmem_slot;
   volatile int abort_flag;
-  int gtile[MAX_GROUPS + 1];  // exclusive prefix of 128-row tiles per group
-  int grow[MAX_GROUPS + 1];   // first row of each group (and the end row)
+  grp::Table tb;
 };
 
-__device__ __forceinline__ bool wait_or_abort(Shared& s, uint64_t* bar, uint32_t parity, const Args& a) {
-  if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (s.abort_flag) return false;
-    if (clock64() - t0 > a.wait_limit) {
-      s.abort_flag = 1;
-      atomicOr(a.status, MOE_STATUS_WAIT_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-struct Tile {
-  int g, m_tile, n_tile, a_row, rows;
-};
-
-__device__ __forceinline__ Tile decode(const Shared& s, int G, int n_tiles, int tile) {
-  int q = tile / n_tiles;
-  int lo = 0, hi = G - 1;  // last g with gtile[g] <= q
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (s.gtile[mid] <= q)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  Tile t;
-  t.g = lo;
-  int local = tile - s.gtile[lo] * n_tiles;
-  int mtc = s.gtile[lo + 1] - s.gtile[lo];
-  t.n_tile = local / mtc;
-  t.m_tile = local - t.n_tile * mtc;
-  t.a_row = s.grow[lo] + t.m_tile * BM;
-  int m = s.grow[lo + 1] - s.grow[lo];
-  t.rows = min(BM, m - t.m_tile * BM);
-  return t;
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+using grp::silu;
+using grp::Tile;
+using grp::wait_or_abort;
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -138,40 +99,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.E + args.shared;
 
-  // ---- set-up: tile prefix over groups, barriers, TMEM
+  // ---- set-up: tile table over groups, barriers, TMEM
   if (warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < G; base += 32) {
-      int g = base + lane;
-      int row0 = 0, m = 0;
-      if (g < G) {
-        if (args.offsets == nullptr) {  // one group: rows [0, T)
-          row0 = 0;
-          m = args.T;
-        } else if (g < args.E) {
-          row0 = args.offsets[g];
-          m = args.offsets[g + 1] - row0;
-        } else {
-          row0 = args.R;
-          m = args.T;
-        }
-      }
-      int mt = (m + BM - 1) / BM;
-      int incl = mt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (g < G) {
-        s.gtile[g] = carry + incl - mt;
-        s.grow[g] = row0;
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
+    grp::build_table(s.tb, args.offsets, args.E, args.shared, args.R, args.T, BM, lane);
     if (lane == 0) {
-      s.gtile[G] = carry;
-      s.grow[G] = args.offsets == nullptr ? args.T : (args.shared ? args.R + args.T : args.offsets[args.E]);
       for (int i = 0; i < STAGES; ++i) {
         mbar_init(&s.full[i], 1);
         mbar_init(&s.empty[i], 1);
@@ -196,7 +127,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_slot;
-  const int total = s.gtile[G] * args.n_tiles;
+  const int total = s.tb.gtile[G] * args.n_tiles;
   const int kpb = args.K / BK;  // K blocks per pass over A
   const int kblocks = kpb * args.ksplit;
 
@@ -207,7 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     long long issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      Tile t = decode(s, G, args.n_tiles, tile);
+      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
       const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
       const int zg = t.g < args.E ? t.g : 0;
       int n0, n1;
@@ -222,7 +153,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         n1 = n0 + BN / 2;
       }
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_or_abort(s, &s.empty[stage], phase ^ 1, args)) {
+        if (!wait_or_abort(&s.empty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
           break;
         }
@@ -267,14 +198,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int kb = 0; kb < kblocks; ++kb) {
         const int kc = kb % ch_len;
         if (kc == 0) {
-          if (!wait_or_abort(s, &s.tempty[acc], acc_phase ^ 1, args)) {
+          if (!wait_or_abort(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
             ok = false;
             break;
           }
           tc_fence_after();
           d = tmem_base + (uint32_t)(acc * BN);
         }
-        if (!wait_or_abort(s, &s.full[stage], phase, args)) {
+        if (!wait_or_abort(&s.full[stage], phase, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
           break;
         }
@@ -308,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      Tile t = decode(s, G, args.n_tiles, tile);
+      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
       if (args.mode == 2) {
         // router: sum the TMEM chunk partials of this tile in fp32 registers, then store
         float run[BN / 2];
@@ -318,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool fine = true;
         for (int ch = 0; ch < nch; ++ch) {
           int ok = 1;
-          if (lane == 0) ok = wait_or_abort(s, &s.tfull[acc], acc_phase, args);
+          if (lane == 0) ok = wait_or_abort(&s.tfull[acc], acc_phase, &s.abort_flag, args.status, args.wait_limit);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
             fine = false;
@@ -358,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // one lane waits, the warp follows: the tcgen05.ld below is warp-collective
       int ok = 1;
-      if (lane == 0) ok = wait_or_abort(s, &s.tfull[acc], acc_phase, args);
+      if (lane == 0) ok = wait_or_abort(&s.tfull[acc], acc_phase, &s.abort_flag, args.status, args.wait_limit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       __syncwarp();
@@ -429,11 +360,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 // host side
 // ------------------------------------------------------------------------------------------
 namespace {
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+}  // namespace
 
-cudaError_t get_encoder() {
+cudaError_t tma_encoder_ready() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -445,9 +376,8 @@ cudaError_t get_encoder() {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// [rows, K] row-major matrix of `elem`-byte elements; box = box_rows x (128 bytes of K).
-bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t rows, int64_t K,
-               int box_rows) {
+bool tma_encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t rows, int64_t K,
+                   int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(K * elem)};
   cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
@@ -457,9 +387,8 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [G, rows, K] row-major stack of matrices; box = 1 x box_rows x (128 bytes of K).
-bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t G, int64_t rows,
-               int64_t K, int box_rows) {
+bool tma_encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t G, int64_t rows,
+                   int64_t K, int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)G};
   cuuint64_t strides[2] = {(cuuint64_t)(K * elem), (cuuint64_t)(rows * K * elem)};
   cuuint32_t box[3] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows, 1};
@@ -468,8 +397,6 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 int num_sms() {
   static int n = 0;
@@ -482,7 +409,7 @@ int num_sms() {
 }
 
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err) {
-  cudaError_t e = get_encoder();
+  cudaError_t e = tma_encoder_ready();
   if (e != cudaSuccess) {
     *err = "cuTensorMapEncodeTiled is not available from the driver";
     return e;
@@ -500,9 +427,9 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   CUtensorMap tA, tB, tBs;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int ksplit = d.ksplit > 1 ? d.ksplit : 1;
-  bool ok = encode_2d(&tA, d.A, BF, 2, d.a_rows, d.K, gg::BM) &&
-            encode_3d(&tB, d.B, BF, 2, ksplit > 1 ? ksplit : d.E, d.b_rows, d.K, gg::BN / 2) &&
-            encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, gg::BN / 2);
+  bool ok = tma_encode_2d(&tA, d.A, BF, 2, d.a_rows, d.K, gg::BM) &&
+            tma_encode_3d(&tB, d.B, BF, 2, ksplit > 1 ? ksplit : d.E, d.b_rows, d.K, gg::BN / 2) &&
+            tma_encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, gg::BN / 2);
   if (!ok) {
     *err = "cuTensorMapEncodeTiled rejected a grouped-GEMM operand";
     return cudaErrorInvalidValue;

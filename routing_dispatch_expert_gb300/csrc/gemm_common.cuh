@@ -1,0 +1,126 @@
+// Pieces shared by the grouped-GEMM kernels (bf16 and FP8): the per-group tile table built from the
+// device-side expert offsets, the tile decoder of the persistent schedule, the bounded mbarrier wait,
+// and the host-side TMA descriptor encoders.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace grp {
+
+constexpr int MAX_GROUPS = 1025;  // E <= 1024 routed experts + the shared expert
+
+// gtile[g]: exclusive prefix of 128-row tiles over groups; grow[g]: first row of group g (grow[G] =
+// end row). Groups: the E routed experts (rows [offsets[e], offsets[e+1])) and, with a shared expert,
+// group E = rows [R, R + T). offsets == nullptr means one group of rows [0, T).
+struct Table {
+  int gtile[MAX_GROUPS + 1];
+  int grow[MAX_GROUPS + 1];
+};
+
+struct Tile {
+  int g, m_tile, n_tile, a_row, rows;
+};
+
+// Called by one full warp.
+__device__ __forceinline__ void build_table(Table& tb, const int32_t* offsets, int E, int shared, int R, int T,
+                                            int BM, int lane) {
+  const int G = E + shared;
+  int carry = 0;
+  for (int base = 0; base < G; base += 32) {
+    const int g = base + lane;
+    int row0 = 0, m = 0;
+    if (g < G) {
+      if (offsets == nullptr) {
+        row0 = 0;
+        m = T;
+      } else if (g < E) {
+        row0 = offsets[g];
+        m = offsets[g + 1] - row0;
+      } else {
+        row0 = R;
+        m = T;
+      }
+    }
+    const int mt = (m + BM - 1) / BM;
+    int incl = mt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (g < G) {
+      tb.gtile[g] = carry + incl - mt;
+      tb.grow[g] = row0;
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    tb.gtile[G] = carry;
+    tb.grow[G] = offsets == nullptr ? T : (shared ? R + T : offsets[E]);
+  }
+}
+
+// Tile order: group-major, then output-column tile, then 128-row tile.
+__device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int tile, int BM) {
+  const int q = tile / n_tiles;
+  int lo = 0, hi = G - 1;  // last g with gtile[g] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tb.gtile[mid] <= q)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  Tile t;
+  t.g = lo;
+  const int local = tile - tb.gtile[lo] * n_tiles;
+  const int mtc = tb.gtile[lo + 1] - tb.gtile[lo];
+  t.n_tile = local / mtc;
+  t.m_tile = local - t.n_tile * mtc;
+  t.a_row = tb.grow[lo] + t.m_tile * BM;
+  const int m = tb.grow[lo + 1] - tb.grow[lo];
+  t.rows = min(BM, m - t.m_tile * BM);
+  return t;
+}
+
+// Bounded wait on an mbarrier phase. Gives up when another role of the CTA has aborted, or after
+// `limit` SM clocks (then it raises the CTA's abort flag and records MOE_STATUS_WAIT_TIMEOUT).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                              long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(status, MOE_STATUS_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bounded drain used on the way out (normal or aborted): wait for a phase, give up after `limit`.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < limit) {
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+}  // namespace grp
+
+// host: TMA descriptors (gemm.cu)
+cudaError_t tma_encoder_ready();
+// [rows, K] row-major, `elem`-byte elements; box = box_rows x 128 bytes of K, 128-byte swizzle.
+bool tma_encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t rows, int64_t K,
+                   int box_rows);
+// [G, rows, K] row-major stack; box = 1 x box_rows x 128 bytes of K, 128-byte swizzle.
+bool tma_encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t G, int64_t rows,
+                   int64_t K, int box_rows);
+
+}  // namespace moe

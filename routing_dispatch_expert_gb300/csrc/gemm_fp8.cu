@@ -1,0 +1,366 @@
+// FP8 block-scaled grouped GEMM of the expert FFN (tcgen05 kind::f8f6f4, TMEM, TMA).
+//
+// Perplexity blog "Lower latency and higher throughput with multi-node DeepSeek deployment",
+// "Quantization": weights are quantised statically per 128x128 tile, activations at run time per
+// 1x128 vector along K, so a product [M, K] x [K, N] needs the scales (M x K/128) and
+// (K/128 x N/128); the activation scales vary only along K. The SiLU output is itself block
+// quantised with a 128-element amax before the down projection. Same grouping as the bf16 kernel:
+//   mode 0  H (e4m3, 1x128 scales) = quant( silu(A W_gate^T) * (A W_up^T) )
+//   mode 1  yd (bf16)              = (A W_down^T) * row_weight
+// with A = e4m3 rows [R_tot, K] and per-row scales [R_tot, K/128].
+//
+// One 128-deep K block is exactly one scale block, so the tensor core computes each K block's
+// product in a fresh TMEM partial (2 x 256 columns, double buffered) and eight epilogue warps promote
+// it: acc += partial * sa[row, kb] * sb[n_block, kb], in fp32 registers (128 per thread; two warps
+// share each TMEM lane quarter, one per half of the columns). The MMA of block kb+1 overlaps the
+// promotion of block kb.
+//   * mode 0: each thread holds 64 gate and the 64 matching up columns of its row, so SwiGLU is local;
+//     the 128-column amax of H is shared between the two warps of a row through shared memory and a
+//     bounded mbarrier (never a blocking bar.sync, so a timed-out warp cannot hang the others).
+//   * persistent, one CTA per SM, 4-stage TMA ring of 48 KB (A 128 x 128 B, B 256 x 128 B), every
+//     wait bounded, the same exit path as the bf16 kernel.
+#include <cuda.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace g8 {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // e4m3 elements per 128-byte swizzled row = one scale block along K
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+
+struct Args {
+  const int32_t* offsets;
+  int E, shared, R, T, K, n_tiles, mode, I, ldo;
+  void* out;               // mode 0: H codes [R_tot, I]; mode 1: yd bf16 [R_tot, ldo]
+  float* out_scales;       // mode 0: H scales [R_tot, I / 128]
+  const float* a_scales;   // [R_tot, K / 128]
+  const float* b_scales;   // routed weights [E, nb, K / 128]
+  const float* bs_scales;  // shared expert [nb, K / 128]
+  int nb;                  // 128-row blocks of the weight
+  const float* row_weight;
+  int* status;
+  long long wait_limit;
+};
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t pfull[2];
+  uint64_t pempty[2];
+  uint64_t xchg;
+  uint64_t mma_done;
+  uint32_t tmem_slot;
+  volatile int abort_flag;
+  float amax[2][2][BM];  // [tile parity][column half][row]
+  grp::Table tb;
+};
+
+using grp::wait_or_abort;
+
+__global__ void __maxnreg__(200)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmBs, const Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared s;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.E + args.shared;
+
+  if (warp == 0) {
+    grp::build_table(s.tb, args.offsets, args.E, args.shared, args.R, args.T, BM, lane);
+    if (lane == 0) {
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(&s.full[i], 1);
+        mbar_init(&s.empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&s.pfull[i], 1);
+        mbar_init(&s.pempty[i], EPI_WARPS);
+      }
+      mbar_init(&s.xchg, EPI_WARPS);
+      mbar_init(&s.mma_done, 1);
+      s.abort_flag = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmBs);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_slot;
+  const int total = s.tb.gtile[G] * args.n_tiles;
+  const int kblocks = args.K / BK;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
+      const int z = t.g < args.E ? t.g : 0;
+      int n0, n1;
+      if (args.mode == 0) {
+        n0 = t.n_tile * (BN / 2);
+        n1 = args.I + t.n_tile * (BN / 2);
+      } else {
+        n0 = t.n_tile * BN;
+        n1 = n0 + BN / 2;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&s.empty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = smem + stage * STAGE_BYTES;
+        uint8_t* b = a + A_BYTES;
+        mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
+        tma_load_2d(a, &tmA, &s.full[stage], kb * BK, t.a_row);
+        tma_load_3d(b, mb, &s.full[stage], kb * BK, n0, z);
+        tma_load_3d(b + B_BYTES / 2, mb, &s.full[stage], kb * BK, n1, z);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    const long long first = issued > STAGES ? issued - STAGES : 0;
+    for (long long i = first; i < issued; ++i)
+      grp::drain_wait(&s.full[i % STAGES], (uint32_t)((i / STAGES) & 1), args.wait_limit);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer: one K block per TMEM partial
+    constexpr uint32_t IDESC = idesc_e4m3(BM, BN);
+    int stage = 0, p = 0;
+    uint32_t phase = 0, pphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&s.pempty[p], pphase ^ 1, &s.abort_flag, args.status, args.wait_limit) ||
+            !wait_or_abort(&s.full[stage], phase, &s.abort_flag, args.status, args.wait_limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(p * BN);
+        const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t b = a + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk)
+          umma_f8(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), IDESC, kk != 0);
+        umma_commit(&s.empty[stage]);
+        umma_commit(&s.pfull[p]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        p ^= 1;
+        if (p == 0) pphase ^= 1;
+      }
+    }
+    umma_commit(&s.mma_done);
+    grp::drain_wait(&s.mma_done, 0, args.wait_limit);
+  } else if (warp >= 2) {
+    // ---------------- promotion + epilogue (8 warps)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int col_a = args.mode == 0 ? half * 64 : half * 128;
+    const int col_b = args.mode == 0 ? BN / 2 + half * 64 : half * 128 + 64;
+    const int KB = kblocks;
+    int p = 0, tpar = 0;
+    uint32_t pphase = 0, xphase = 0;
+    bool fine = true;
+    for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
+      const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      const bool valid = r < t.rows;
+      const int64_t row = (int64_t)t.a_row + r;
+      const float* bsc = t.g < args.E ? args.b_scales + (int64_t)t.g * args.nb * KB : args.bs_scales;
+      const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + half;
+      const int nb_hi = args.mode == 0 ? args.I / 128 + t.n_tile : nb_lo;
+      const float* sa_row = args.a_scales + row * KB;
+      const float* sb_lo = bsc + (int64_t)nb_lo * KB;
+      const float* sb_hi = bsc + (int64_t)nb_hi * KB;
+
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      float sa_n = valid ? sa_row[0] : 0.f, sl_n = sb_lo[0], sh_n = sb_hi[0];
+      for (int kb = 0; kb < KB; ++kb) {
+        const float s_lo = sa_n * sl_n, s_hi = sa_n * sh_n;
+        if (kb + 1 < KB) {
+          sa_n = valid ? sa_row[kb + 1] : 0.f;
+          sl_n = sb_lo[kb + 1];
+          sh_n = sb_hi[kb + 1];
+        }
+        int ok = 1;
+        if (lane == 0) ok = wait_or_abort(&s.pfull[p], pphase, &s.abort_flag, args.status, args.wait_limit);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          fine = false;
+          break;
+        }
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(p * BN);
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + col_a + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(__uint_as_float(v[i]), s_lo, acc[c + i]);
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + col_b + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[64 + c + i] = fmaf(__uint_as_float(v[i]), s_hi, acc[64 + c + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.pempty[p]);
+        p ^= 1;
+        if (p == 0) pphase ^= 1;
+      }
+      if (!fine) break;
+
+      if (args.mode == 1) {
+        const float w = (valid && t.g < args.E) ? args.row_weight[row] : 1.0f;
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out) + row * args.ldo +
+                                                t.n_tile * BN + half * 128);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * w, acc[8 * i + 1] * w),
+                                pack_bf16x2(acc[8 * i + 2] * w, acc[8 * i + 3] * w),
+                                pack_bf16x2(acc[8 * i + 4] * w, acc[8 * i + 5] * w),
+                                pack_bf16x2(acc[8 * i + 6] * w, acc[8 * i + 7] * w));
+        }
+      } else {
+        // SwiGLU on this thread's 64 columns, then the row's 128-column amax shared with the other half
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          acc[i] = grp::silu(acc[i]) * acc[64 + i];
+          amax = fmaxf(amax, fabsf(acc[i]));
+        }
+        s.amax[tpar][half][r] = amax;
+        __syncwarp();
+        int ok = 1;
+        if (lane == 0) {
+          mbar_arrive(&s.xchg);
+          ok = wait_or_abort(&s.xchg, xphase, &s.abort_flag, args.status, args.wait_limit);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        xphase ^= 1;
+        if (!ok) break;
+        const float row_amax = fmaxf(s.amax[tpar][0][r], s.amax[tpar][1][r]);
+        tpar ^= 1;
+        const float scale = row_amax > 0.f ? __fdiv_rn(row_amax, 448.0f) : 1.0f;
+        if (valid) {
+          uint32_t q[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            uint32_t w4 = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              w4 |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(acc[4 * i + j], scale), __NV_SATFINITE, __NV_E4M3)
+                    << (8 * j);
+            q[i] = w4;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.out) + row * args.ldo +
+                                                t.n_tile * (BN / 2) + half * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
+          if (half == 0) args.out_scales[row * (args.I / 128) + t.n_tile] = scale;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace g8
+
+cudaError_t launch_grouped_gemm_fp8(const GroupedGemmFp8Desc& d, cudaStream_t stream, std::string* err) {
+  cudaError_t e = tma_encoder_ready();
+  if (e != cudaSuccess) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return e;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(g8::grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             g8::SMEM_BYTES);
+    if (e != cudaSuccess) {
+      *err = "cudaFuncSetAttribute failed";
+      return e;
+    }
+    attr_set = true;
+  }
+  CUtensorMap tA, tB, tBs;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  bool ok = tma_encode_2d(&tA, d.A, U8, 1, d.a_rows, d.K, g8::BM) &&
+            tma_encode_3d(&tB, d.B, U8, 1, d.E, d.b_rows, d.K, g8::BN / 2) &&
+            tma_encode_3d(&tBs, d.Bs ? d.Bs : d.B, U8, 1, 1, d.b_rows, d.K, g8::BN / 2);
+  if (!ok) {
+    *err = "cuTensorMapEncodeTiled rejected an FP8 grouped-GEMM operand";
+    return cudaErrorInvalidValue;
+  }
+  g8::Args a;
+  a.offsets = d.offsets;
+  a.E = d.E;
+  a.shared = d.Bs != nullptr;
+  a.R = d.R;
+  a.T = d.T;
+  a.K = d.K;
+  a.mode = d.mode;
+  a.I = d.I;
+  a.n_tiles = d.mode == 0 ? d.I / (g8::BN / 2) : d.N / g8::BN;
+  a.ldo = d.ldo;
+  a.out = d.out;
+  a.out_scales = d.out_scales;
+  a.a_scales = d.a_scales;
+  a.b_scales = d.b_scales;
+  a.bs_scales = d.Bs ? d.bs_scales : d.b_scales;
+  a.nb = (int)(d.b_rows / 128);
+  a.row_weight = d.row_weight;
+  a.status = d.status;
+  a.wait_limit = 4000000000LL;
+  g8::grouped_gemm_fp8_kernel<<<num_sms(), g8::THREADS, g8::SMEM_BYTES, stream>>>(tA, tB, tBs, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -69,6 +69,28 @@ struct GroupedGemmDesc {
 };
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
 
+// Step 3, FP8 layer: block-scaled grouped GEMM (e4m3 operands, fp32 128x128 weight scales, 1x128
+// activation scales). mode 0: H codes + 1x128 scales; mode 1: yd bf16 x row_weight.
+struct GroupedGemmFp8Desc {
+  const void* A;  // [a_rows, K] e4m3
+  const float* a_scales;  // [a_rows, K/128]
+  int64_t a_rows;
+  const void* B;  // [E, b_rows, K] e4m3
+  const float* b_scales;  // [E, b_rows/128, K/128]
+  const void* Bs;  // [b_rows, K] shared expert or nullptr
+  const float* bs_scales;
+  int64_t b_rows;
+  const int32_t* offsets;
+  int E, R, T, K, N, I;
+  int mode;
+  void* out;
+  float* out_scales;
+  int ldo;
+  const float* row_weight;
+  int* status;
+};
+cudaError_t launch_grouped_gemm_fp8(const GroupedGemmFp8Desc& d, cudaStream_t stream, std::string* err);
+
 // Step 4: combine.
 cudaError_t launch_combine(const void* yd, const int32_t* inv_pos, void* y, int T, int h, int k, int shared,
                            cudaStream_t stream);

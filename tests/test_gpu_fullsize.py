@@ -11,7 +11,7 @@ import oracle
 import synth
 import routing_dispatch_expert_gb300 as rde
 from routing_dispatch_expert_gb300 import build as pkg_build
-from harness import BF16_TOL, GpuLayer, bits, cfg_of, oracle_tokens, rel_err_per_token, route_kwargs
+from harness import BF16_TOL, FP8_TOL, GpuLayer, bits, cfg_of, oracle_tokens, rel_err_per_token, route_kwargs
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def _sample(n, count, seed):
     return np.array(sorted(s))
 
 
-@pytest.mark.parametrize("name,n_tok", [("mixtral", 4), ("dsv3_prefill", 8), ("dsv3_decode", 16)])
+@pytest.mark.parametrize("name,n_tok", [("mixtral", 4), ("dsv3_prefill", 8), ("dsv3_decode", 16), ("dsv3_fp8", 8)])
 def test_full_size_layer(name, n_tok):
     wl = synth.WORKLOADS[name]
     L = GpuLayer(wl)
@@ -55,8 +55,16 @@ def test_full_size_layer(name, n_tok):
     np.testing.assert_array_equal(it["row_token"].cpu().numpy(), row_token)
     # dispatch copies of sampled rows: bit-exact
     R = wl.T * wl.k
+    fp8 = wl.dtype == "fp8"
+    tol = FP8_TOL if fp8 else BF16_TOL
     rows = _sample(R, 512, 1)
-    np.testing.assert_array_equal(bits(it["xd"][torch.as_tensor(rows, device="cuda")]), x[row_token[rows]])
+    sel = torch.as_tensor(rows, device="cuda")
+    if fp8:
+        xq, xsc = oracle.quant_1x128(oracle.bf16_to_double(x[row_token[rows]]))
+        np.testing.assert_array_equal(it["xd"][sel].cpu().numpy(), xq)
+        np.testing.assert_array_equal(it["xd_scales"][sel].cpu().numpy(), xsc)
+    else:
+        np.testing.assert_array_equal(bits(it["xd"][sel]), x[row_token[rows]])
     # router GEMM on sampled tokens vs the fp64 oracle
     toks = _sample(wl.T, 32, 2)
     lo = oracle.router_logits(x[toks], L.inp["w_router"].cpu().numpy())
@@ -65,12 +73,12 @@ def test_full_size_layer(name, n_tok):
     toks = _sample(wl.T, n_tok, 3)
     y_ref, o, _ = oracle_tokens(L, toks, idx, w, x)
     e = rel_err_per_token(bits(y[torch.as_tensor(toks, device="cuda")]), y_ref)
-    assert e.max() <= BF16_TOL, f"max rel err {e.max()}"
+    assert e.max() <= tol, f"max rel err {e.max()}"
     # the route-weighted expert rows of those tokens
     yd = oracle.bf16_to_double(bits(it["yd"][torch.as_tensor(inv_pos[toks].ravel(), device="cuda")]))
     ref = (o * w[toks][:, :, None].astype(np.float64)).reshape(-1, wl.h)
     err = np.abs(yd - ref).max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-30)
-    assert err.max() <= BF16_TOL
+    assert err.max() <= tol
     del L
     gc.collect()
     torch.cuda.empty_cache()

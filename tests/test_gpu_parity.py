@@ -8,7 +8,7 @@ import oracle
 import synth
 import routing_dispatch_expert_gb300 as rde
 from routing_dispatch_expert_gb300 import build as pkg_build
-from harness import (BF16_TOL, MARGIN, GpuLayer, bits, cfg_of, oracle_tokens, rel_err_per_token, route_kwargs,
+from harness import (BF16_TOL, FP8_TOL, MARGIN, GpuLayer, bits, cfg_of, oracle_tokens, rel_err_per_token, route_kwargs,
                      selection_margin)
 
 pytestmark = pytest.mark.gpu
@@ -26,6 +26,10 @@ SMALL = {
     # E >= 128: the router GEMM runs on the tensor cores (fp32 weight as three bf16 terms)
     "dsv3_e256": _W["dsv3_prefill"].replace(name="dsv3_e256", T=300, h=512, E=256, I=128, I_shared=128),
     "dsv3_e128_skew": _W["dsv3_decode"].replace(name="dsv3_e128_skew", T=130, h=256, E=128, I=128, I_shared=128),
+    # the FP8 layer: e4m3 experts with 128x128 scales, 1x128 activations, SiLU output requantised
+    "fp8_small": _W["dsv3_fp8"].replace(name="fp8_small", T=300, h=512, E=64, I=256, I_shared=256),
+    "fp8_e256_skew": _W["dsv3_fp8"].replace(name="fp8_e256_skew", T=257, h=256, E=256, I=128, I_shared=128),
+    "fp8_noshared": _W["dsv3_fp8"].replace(name="fp8_noshared", T=129, h=512, E=32, I=384, I_shared=0),
 }
 
 
@@ -70,24 +74,35 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
     rw = it["row_weight"].cpu().numpy()
     np.testing.assert_array_equal(rw[ref["inv_pos"].ravel()], it["topk_w"].cpu().numpy().ravel())
     R = wl.T * wl.k
-    xd = bits(it["xd"])
-    np.testing.assert_array_equal(xd[:R], ref["xd"])
-    if wl.has_shared:
-        np.testing.assert_array_equal(xd[R:], x)
+    fp8 = wl.dtype == "fp8"
+    tol = FP8_TOL if fp8 else BF16_TOL
+    if fp8:  # codes and 1x128 scales of the dispatched rows are decided identically: bit-exact
+        xd = it["xd"].cpu().numpy()
+        xs = it["xd_scales"].cpu().numpy()
+        np.testing.assert_array_equal(xd[:R], ref["xd"])
+        np.testing.assert_array_equal(xs[:R], ref["xd_scales"])
+        if wl.has_shared:
+            np.testing.assert_array_equal(xd[R:], ref["xq"])
+            np.testing.assert_array_equal(xs[R:], ref["xs"])
+    else:
+        xd = bits(it["xd"])
+        np.testing.assert_array_equal(xd[:R], ref["xd"])
+        if wl.has_shared:
+            np.testing.assert_array_equal(xd[R:], x)
 
     # expert outputs per row (route-weighted), and the shared expert's rows
     yd = oracle.bf16_to_double(bits(it["yd"]))
     o_w = ref["o_rows"] * rw[:, None].astype(np.float64)
     err = np.abs(yd[:R] - o_w).max(axis=1) / np.maximum(np.abs(o_w).max(axis=1), 1e-30)
-    assert err.max() <= BF16_TOL, f"routed rows: max rel err {err.max()}"
+    assert err.max() <= tol, f"routed rows: max rel err {err.max()}"
     if wl.has_shared:
         s = ref["shared_out"]
         err = np.abs(yd[R:] - s).max(axis=1) / np.maximum(np.abs(s).max(axis=1), 1e-30)
-        assert err.max() <= BF16_TOL, f"shared rows: max rel err {err.max()}"
+        assert err.max() <= tol, f"shared rows: max rel err {err.max()}"
 
     # layer output, every token
     e = rel_err_per_token(bits(y), ref["y"])
-    assert e.max() <= BF16_TOL, f"y: max rel err {e.max()} at token {e.argmax()}"
+    assert e.max() <= tol, f"y: max rel err {e.max()} at token {e.argmax()}"
 
     # routing on the oracle's own fp64 logits agrees wherever the decision is not a near-tie
     idx2, _ = oracle.route(lo, bias, **route_kwargs(wl))
