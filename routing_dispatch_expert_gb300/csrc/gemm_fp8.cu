@@ -70,7 +70,7 @@ struct Shared {
 
 using grp::wait_or_abort;
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmBs, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -225,20 +225,20 @@ __global__ void __maxnreg__(200)
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(p * BN);
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + col_a + c, v);
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(taddr + col_a + c, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(__uint_as_float(v[i]), s_lo, acc[c + i]);
+          for (int i = 0; i < 16; ++i) acc[c + i] = fmaf(__uint_as_float(v[i]), s_lo, acc[c + i]);
         }
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + col_b + c, v);
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(taddr + col_b + c, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[64 + c + i] = fmaf(__uint_as_float(v[i]), s_hi, acc[64 + c + i]);
+          for (int i = 0; i < 16; ++i) acc[64 + c + i] = fmaf(__uint_as_float(v[i]), s_hi, acc[64 + c + i]);
         }
         tc_fence_before();
         __syncwarp();
