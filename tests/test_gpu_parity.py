@@ -64,7 +64,7 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
     assert np.abs(logits - lo).max() <= 1e-5 * np.abs(lo).max() + 1e-6
 
     # the whole layer on identical logits
-    ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, **route_kwargs(wl))
+    ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, fp8=wl.dtype == "fp8", **route_kwargs(wl))
     np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), ref["topk_idx"])
     np.testing.assert_allclose(it["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-6, atol=1e-7)
     np.testing.assert_array_equal(it["counts"].cpu().numpy(), ref["counts"])
