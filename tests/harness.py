@@ -31,6 +31,13 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def logit_tolerance(x_bits: np.ndarray, w_r: np.ndarray) -> np.ndarray:
+    """Allowed |logit error| per (token, expert) of an fp32-accumulated router GEMM: 2^-16 of
+    sum_d |x_d w_d| (the scale at which the accumulation rounds; the plain max|logit| is the wrong
+    scale when the terms cancel), computed by the oracle on the absolute values."""
+    return 2.0 ** -16 * oracle.router_logits(x_bits & np.uint16(0x7FFF), np.abs(w_r)).astype(np.float64) + 1e-6
+
+
 def rel_err_per_token(y_bits: np.ndarray, ref_bits_or_double: np.ndarray) -> np.ndarray:
     y = oracle.bf16_to_double(y_bits)
     ref = (oracle.bf16_to_double(ref_bits_or_double) if ref_bits_or_double.dtype == np.uint16
