@@ -10,12 +10,13 @@
 // with A = e4m3 rows [R_tot, K] and per-row scales [R_tot, K/128].
 //
 // One 128-deep K block is exactly one scale block, so the tensor core computes each K block's
-// product in a fresh TMEM partial (2 x 256 columns, double buffered) and eight epilogue warps promote
-// it: acc += partial * sa[row, kb] * sb[n_block, kb], in fp32 registers (128 per thread; two warps
-// share each TMEM lane quarter, one per half of the columns). The MMA of block kb+1 overlaps the
-// promotion of block kb.
-//   * mode 0: each thread holds 64 gate and the 64 matching up columns of its row, so SwiGLU is local;
-//     the 128-column amax of H is shared between the two warps of a row through shared memory and a
+// product in a fresh TMEM partial (2 x 256 columns, double buffered) and sixteen epilogue warps
+// promote it: acc += partial * sa[row, kb] * sb[n_block, kb], in fp32 registers (64 per thread; four
+// warps share each TMEM lane quarter, one per quarter of the columns; two accumulators per packed
+// fma.rn.f32x2). The MMA of block kb+1 overlaps the promotion of block kb; four promotion warps per
+// SM sub-partition hide the TMEM-load latency.
+//   * mode 0: each thread holds 32 gate and the 32 matching up columns of its row, so SwiGLU is local;
+//     the 128-column amax of H is shared by the four warps of a row through shared memory and a
 //     bounded mbarrier (never a blocking bar.sync, so a timed-out warp cannot hang the others).
 //   * persistent, one CTA per SM, 4-stage TMA ring of 48 KB (A 128 x 128 B, B 256 x 128 B), every
 //     wait bounded, the same exit path as the bf16 kernel.
@@ -36,7 +37,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;
+constexpr int PARTS = EPI_WARPS / 4;  // column parts per TMEM lane quarter
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
@@ -64,11 +66,20 @@ struct Shared {
   uint64_t mma_done;
   uint32_t tmem_slot;
   volatile int abort_flag;
-  float amax[2][2][BM];  // [tile parity][column half][row]
+  float amax[2][PARTS][BM];  // [tile parity][column part][row]
   grp::Table tb;
 };
 
 using grp::wait_or_abort;
+
+// acc0 += v0 * s, acc1 += v1 * s (two IEEE fma, one instruction)
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float v0, float v1, float s) {
+  asm("{\n\t.reg .b64 ra, rv, rs;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rv, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\t"
+      "fma.rn.f32x2 ra, rv, rs, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(v0), "f"(v1), "f"(s));
+}
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -182,12 +193,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     umma_commit(&s.mma_done);
     grp::drain_wait(&s.mma_done, 0, args.wait_limit);
   } else if (warp >= 2) {
-    // ---------------- promotion + epilogue (8 warps)
+    // ---------------- promotion + epilogue (16 warps)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int col_a = args.mode == 0 ? half * 64 : half * 128;
-    const int col_b = args.mode == 0 ? BN / 2 + half * 64 : half * 128 + 64;
+    // mode 0: gate columns [32 part, +32) and the matching up columns; mode 1: columns [64 part, +64)
+    const int col_a = args.mode == 0 ? part * 32 : part * 64;
+    const int col_b = args.mode == 0 ? BN / 2 + part * 32 : part * 64 + 32;
     const int KB = kblocks;
     int p = 0, tpar = 0;
     uint32_t pphase = 0, xphase = 0;
@@ -196,24 +208,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
       const bool valid = r < t.rows;
       const int64_t row = (int64_t)t.a_row + r;
-      const float* bsc = t.g < args.E ? args.b_scales + (int64_t)t.g * args.nb * KB : args.bs_scales;
-      const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + half;
+      // scale indices (32-bit: R_tot * K/128 and E * nb * K/128 stay far below 2^31)
+      const float* bsc = t.g < args.E ? args.b_scales : args.bs_scales;
+      const int gbase = t.g < args.E ? t.g * args.nb * KB : 0;
+      const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + (part >> 1);
       const int nb_hi = args.mode == 0 ? args.I / 128 + t.n_tile : nb_lo;
-      const float* sa_row = args.a_scales + row * KB;
-      const float* sb_lo = bsc + (int64_t)nb_lo * KB;
-      const float* sb_hi = bsc + (int64_t)nb_hi * KB;
+      const int ia = (int)row * KB;
+      const int il = gbase + nb_lo * KB;
+      const int ih = gbase + nb_hi * KB;
 
-      float acc[128];
+      float acc[64];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      float sa_n = valid ? sa_row[0] : 0.f, sl_n = sb_lo[0], sh_n = sb_hi[0];
+      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      float sa_n = valid ? args.a_scales[ia] : 0.f;  // the row scale is prefetched one K block ahead
       for (int kb = 0; kb < KB; ++kb) {
-        const float s_lo = sa_n * sl_n, s_hi = sa_n * sh_n;
-        if (kb + 1 < KB) {
-          sa_n = valid ? sa_row[kb + 1] : 0.f;
-          sl_n = sb_lo[kb + 1];
-          sh_n = sb_hi[kb + 1];
-        }
+        const float s_lo = sa_n * bsc[il + kb], s_hi = sa_n * bsc[ih + kb];
+        if (kb + 1 < KB) sa_n = valid ? args.a_scales[ia + kb + 1] : 0.f;
         int ok = 1;
         if (lane == 0) ok = wait_or_abort(&s.pfull[p], pphase, &s.abort_flag, args.status, args.wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -225,20 +235,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(p * BN);
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < 32; c += 16) {
           uint32_t v[16];
           tmem_ld16(taddr + col_a + c, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[c + i] = fmaf(__uint_as_float(v[i]), s_lo, acc[c + i]);
+          for (int i = 0; i < 16; i += 2)
+            ffma2(acc[c + i], acc[c + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s_lo);
         }
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < 32; c += 16) {
           uint32_t v[16];
           tmem_ld16(taddr + col_b + c, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[64 + c + i] = fmaf(__uint_as_float(v[i]), s_hi, acc[64 + c + i]);
+          for (int i = 0; i < 16; i += 2)
+            ffma2(acc[32 + c + i], acc[32 + c + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s_hi);
         }
         tc_fence_before();
         __syncwarp();
@@ -252,23 +264,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float w = (valid && t.g < args.E) ? args.row_weight[row] : 1.0f;
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.out) + row * args.ldo +
-                                                t.n_tile * BN + half * 128);
+                                                t.n_tile * BN + part * 64);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 8; ++i)
             dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * w, acc[8 * i + 1] * w),
                                 pack_bf16x2(acc[8 * i + 2] * w, acc[8 * i + 3] * w),
                                 pack_bf16x2(acc[8 * i + 4] * w, acc[8 * i + 5] * w),
                                 pack_bf16x2(acc[8 * i + 6] * w, acc[8 * i + 7] * w));
         }
       } else {
-        // SwiGLU on this thread's 64 columns, then the row's 128-column amax shared with the other half
+        // SwiGLU on this thread's 32 columns, then the row's 128-column amax shared by the four parts
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          acc[i] = grp::silu(acc[i]) * acc[64 + i];
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = grp::silu(acc[i]) * acc[32 + i];
           amax = fmaxf(amax, fabsf(acc[i]));
         }
-        s.amax[tpar][half][r] = amax;
+        s.amax[tpar][part][r] = amax;
         __syncwarp();
         int ok = 1;
         if (lane == 0) {
@@ -279,13 +291,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         xphase ^= 1;
         if (!ok) break;
-        const float row_amax = fmaxf(s.amax[tpar][0][r], s.amax[tpar][1][r]);
+        float row_amax = s.amax[tpar][0][r];
+#pragma unroll
+        for (int q = 1; q < PARTS; ++q) row_amax = fmaxf(row_amax, s.amax[tpar][q][r]);
         tpar ^= 1;
         const float scale = row_amax > 0.f ? __fdiv_rn(row_amax, 448.0f) : 1.0f;
         if (valid) {
-          uint32_t q[16];
+          uint32_t q[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < 8; ++i) {
             uint32_t w4 = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -294,10 +308,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             q[i] = w4;
           }
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.out) + row * args.ldo +
-                                                t.n_tile * (BN / 2) + half * 64);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
-          if (half == 0) args.out_scales[row * (args.I / 128) + t.n_tile] = scale;
+                                                t.n_tile * (BN / 2) + part * 32);
+          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+          if (part == 0) args.out_scales[row * (args.I / 128) + t.n_tile] = scale;
         }
       }
     }
