@@ -28,9 +28,6 @@
 //     buffered so the epilogue of one tile overlaps the MMAs of the next);
 //   * for mode 0 the B tile holds 128 gate rows and the 128 matching up rows, so the SwiGLU product
 //     is formed in the epilogue and only H is written;
-//   * the last, partial 128-row tile of a group is computed transposed (weight rows as M = 128,
-//     activation rows as N = rows rounded up to 16), so ragged expert segments cost at most 15
-//     padded rows instead of up to 127;
 //   * every mbarrier wait is bounded; on a time-out the kernel records MOE_STATUS_WAIT_TIMEOUT,
 //     drains its own copies and MMAs (again bounded), frees TMEM and returns.
 #include <cuda.h>
@@ -198,11 +195,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       uint32_t d = 0;
-      // A tail tile (fewer than 128 rows) is computed transposed: the two 128-row weight boxes are
-      // the M = 128 operand and the activation rows the N operand, N = rows rounded up to 16.
-      const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
-      const bool swap = args.mode != 2 && t.rows < BM;
-      const uint32_t idesc_swap = idesc_bf16(BM, (t.rows + 15) & ~15);
       for (int kb = 0; kb < kblocks; ++kb) {
         const int kc = kb % ch_len;
         if (kc == 0) {
@@ -220,18 +212,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t b = a + A_BYTES;
-        if (swap) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t xdesc = sw128_kmajor_desc(a + kk * 32);
-            umma_f16(d, sw128_kmajor_desc(b + kk * 32), xdesc, idesc_swap, (kc | kk) != 0);
-            umma_f16(d + BN / 2, sw128_kmajor_desc(b + B_BYTES / 2 + kk * 32), xdesc, idesc_swap, (kc | kk) != 0);
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), idesc, (kc | kk) != 0);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_f16(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), idesc, (kc | kk) != 0);
         umma_commit(&s.empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
@@ -311,54 +294,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      if (t.rows < BM) {
-        // transposed tail tile: TMEM lane = weight row r of a box, column j = activation row
-        const int n16 = (t.rows + 15) & ~15;
-        __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(args.out);
-        if (args.mode == 0) {
-          const int64_t col = (int64_t)t.n_tile * (BN / 2) + r;  // H column
-#pragma unroll 1
-          for (int j0 = 0; j0 < n16; j0 += 16) {
-            uint32_t g[16], u[16];
-            tmem_ld16(taddr + j0, g);
-            tmem_ld16(taddr + BN / 2 + j0, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (j0 + i < t.rows)
-                outp[((int64_t)t.a_row + j0 + i) * args.ldo + col] =
-                    __float2bfloat16_rn(silu(__uint_as_float(g[i])) * __uint_as_float(u[i]));
-          }
-        } else {
-#pragma unroll 1
-          for (int box = 0; box < 2; ++box) {
-            const int64_t col = (int64_t)t.n_tile * BN + box * (BN / 2) + r;
-#pragma unroll 1
-            for (int j0 = 0; j0 < n16; j0 += 16) {
-              uint32_t v[16];
-              tmem_ld16(taddr + box * (BN / 2) + j0, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int j = j0 + i;
-                if (j < t.rows) {
-                  const float w = t.g < args.E ? args.row_weight[t.a_row + j] : 1.0f;
-                  outp[((int64_t)t.a_row + j) * args.ldo + col] = __float2bfloat16_rn(__uint_as_float(v[i]) * w);
-                }
-              }
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
-        continue;
-      }
       const bool valid = r < t.rows;
       const int64_t orow = (int64_t)t.a_row + r;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (args.mode == 0) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * (BN / 2);
 #pragma unroll 1
