@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     long long issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM, args.mode == 2);
       const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
       const int zg = t.g < args.E ? t.g : 0;
       int n0, n1;
@@ -159,8 +159,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint8_t* a = smem + stage * STAGE_BYTES;
         uint8_t* b = a + A_BYTES;
-        const int pass = kb / kpb;
-        const int ka = (kb - pass * kpb) * BK;
+        // router: the three weight terms of one K block are consecutive stages, so the A tile is
+        // re-read from L2 right away instead of once per full pass over K
+        const int pass = args.ksplit > 1 ? kb % args.ksplit : 0;
+        const int ka = (args.ksplit > 1 ? kb / args.ksplit : kb) * BK;
         const int z = args.ksplit > 1 ? pass : zg;
         mbar_arrive_expect_tx(&s.full[stage], n1 >= 0 ? STAGE_BYTES : A_BYTES + B_BYTES / 2);
         tma_load_2d(a, &tmA, &s.full[stage], ka, t.a_row);
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM, args.mode == 2);
       if (args.mode == 2) {
         // router: sum the TMEM chunk partials of this tile in fp32 registers, then store
         float run[BN / 2];

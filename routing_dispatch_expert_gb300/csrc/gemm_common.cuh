@@ -63,8 +63,10 @@ __device__ __forceinline__ void build_table(Table& tb, const int32_t* offsets, i
   }
 }
 
-// Tile order: group-major, then output-column tile, then 128-row tile.
-__device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int tile, int BM) {
+// Tile order: group-major, then output-column tile, then 128-row tile (so the CTAs running together
+// share one weight tile through L2); n_inner swaps the last two (the router: the activation rows are
+// the large operand).
+__device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int tile, int BM, bool n_inner = false) {
   const int q = tile / n_tiles;
   int lo = 0, hi = G - 1;  // last g with gtile[g] <= q
   while (lo < hi) {
@@ -78,8 +80,13 @@ __device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int 
   t.g = lo;
   const int local = tile - tb.gtile[lo] * n_tiles;
   const int mtc = tb.gtile[lo + 1] - tb.gtile[lo];
-  t.n_tile = local / mtc;
-  t.m_tile = local - t.n_tile * mtc;
+  if (n_inner) {
+    t.m_tile = local / n_tiles;
+    t.n_tile = local - t.m_tile * n_tiles;
+  } else {
+    t.n_tile = local / mtc;
+    t.m_tile = local - t.n_tile * mtc;
+  }
   t.a_row = tb.grow[lo] + t.m_tile * BM;
   const int m = tb.grow[lo + 1] - tb.grow[lo];
   t.rows = min(BM, m - t.m_tile * BM);

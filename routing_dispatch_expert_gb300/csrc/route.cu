@@ -10,7 +10,9 @@
 // Readings where the pages are silent: the group score is the sum of the two largest biased scores
 // of the group; ties go to the lower expert (and group) index; the sigmoid is evaluated in fp64 and
 // rounded once to fp32, and the selection key is that fp32 value plus the bias in fp32, so the
-// selection is a deterministic function of the fp32 logits; softmax layers select on the logits.
+// selection is a deterministic function of the fp32 logits (the kernel decides on fp32-evaluated keys
+// and re-decides on the exact ones whenever a gap is too small to be certain); softmax layers select
+// on the logits.
 #include <float.h>
 
 #include "common.cuh"
@@ -173,117 +175,164 @@ __device__ __forceinline__ void warp_argmax(float& v, int& e, float& s) {
   }
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// The selection key of the sigmoid layers is fp32(sigmoid(l)) + bias with the sigmoid evaluated in
+// fp64 and rounded once. The fast pass evaluates it in fp32 (expf, at most 2 ulp, then two correctly
+// rounded operations): |key_fast - key| < 4e-7. A decision taken on the fast keys is the decision on
+// the exact keys whenever every deciding gap exceeds twice the error; the thresholds below are ten
+// times that. A token with a smaller gap is selected again on the exact fp64 keys.
+constexpr float kKeyGap = 4e-6f;    // between two expert keys
+constexpr float kGroupGap = 1e-5f;  // between two group scores (sums of two keys)
+
+__device__ __forceinline__ float sigmoid_exact(float l) { return __double2float_rn(1.0 / (1.0 + exp(-(double)l))); }
+__device__ __forceinline__ float sigmoid_fast(float l) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l))); }
+
+// Group stage and expert stage on the keys of one token. Returns in sel_e / sel_l (lanes < k) the
+// chosen experts in descending key order and their logits. *clear is false when a deciding gap is
+// below the thresholds (only tracked when track_gaps).
+template <int EPL>
+__device__ __forceinline__ void select_experts(const TopkDesc& d, const float (&key)[EPL], const float (&lv)[EPL],
+                                               const bool (&valid)[EPL], int lane, int gs, bool track_gaps,
+                                               int& sel_e, float& sel_l, bool& clear) {
+  clear = true;
+  uint32_t kept = 0xffffffffu;
+  if (d.n_group > 1) {
+    float my_gscore = -INFINITY;
+    for (int g = 0; g < d.n_group; ++g) {
+      float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane * EPL + i;
+        if (valid[i] && e / gs == g) {
+          const float v = key[i];
+          if (v > t1) {
+            t2 = t1;
+            t1 = v;
+          } else if (v > t2) {
+            t2 = v;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+        const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+        const float n1 = fmaxf(t1, o1);
+        t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+        t1 = n1;
+      }
+      const float sc = gs >= 2 ? __fadd_rn(t1, t2) : t1;
+      if (lane == g) my_gscore = sc;
+    }
+    kept = 0;
+    for (int r = 0; r < d.topk_group; ++r) {
+      const bool cand = lane < d.n_group && !((kept >> lane) & 1u);
+      float v = cand ? my_gscore : -INFINITY;
+      int gi = cand ? lane : 64 + lane;
+      float dummy = 0.f;
+      warp_argmax(v, gi, dummy);
+      kept |= 1u << (gi & 31);
+    }
+    if (track_gaps && d.topk_group < d.n_group) {
+      const bool in = lane < d.n_group && ((kept >> lane) & 1u);
+      const bool out = lane < d.n_group && !((kept >> lane) & 1u);
+      const float kept_min = warp_min(in ? my_gscore : INFINITY);
+      const float rest_max = warp_max(out ? my_gscore : -INFINITY);
+      if (!(kept_min - rest_max > kGroupGap)) clear = false;
+    }
+  }
+  uint32_t taken = 0;
+  sel_e = 0;
+  sel_l = 0.f;
+  float prev = 0.f;
+  const int rounds = track_gaps ? d.k + 1 : d.k;  // one more round finds the best key left out
+  for (int j = 0; j < rounds; ++j) {
+    float bv = -INFINITY, bl = 0.f;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane * EPL + i;
+      const bool ok = valid[i] && !((taken >> i) & 1u) && ((kept >> (e / gs)) & 1u);
+      if (ok && (key[i] > bv || be == 0x7fffffff)) {
+        bv = key[i];
+        be = e;
+        bl = lv[i];
+      }
+    }
+    warp_argmax(bv, be, bl);
+    if (track_gaps && j > 0 && !(prev - bv > kKeyGap)) clear = false;
+    prev = bv;
+    if (j == d.k) break;  // the (k+1)-th key only checks the gap
+    if (be / EPL == lane) taken |= 1u << (be - lane * EPL);
+    if (lane == j) {
+      sel_e = be;
+      sel_l = bl;
+    }
+  }
+}
+
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int gs = d.E / d.n_group;
+  const bool sigmoid = d.score == MOE_SCORE_SIGMOID;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.T; t += warps) {
     const float* lrow = d.logits + (int64_t)t * d.E;
-    float key[EPL], sv[EPL];
+    float key[EPL], lv[EPL], bias[EPL];
     bool valid[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane * EPL + i;
       valid[i] = e < d.E;
-      float l = valid[i] ? lrow[e] : 0.f;
-      float s, kv;
-      if (d.score == MOE_SCORE_SOFTMAX) {
-        s = l;
-        kv = l;
-      } else {
-        s = __double2float_rn(1.0 / (1.0 + exp(-(double)l)));
-        kv = d.bias ? __fadd_rn(s, d.bias[valid[i] ? e : 0]) : s;
-      }
+      lv[i] = valid[i] ? lrow[e] : 0.f;
+      bias[i] = (sigmoid && d.bias && valid[i]) ? d.bias[e] : 0.f;
+      float kv = sigmoid ? __fadd_rn(sigmoid_fast(lv[i]), bias[i]) : lv[i];
       if (kv != kv) kv = -INFINITY;  // NaN never wins
-      sv[i] = s;
       key[i] = valid[i] ? kv : -INFINITY;
     }
-
-    // group stage
-    uint32_t kept = 0xffffffffu;
-    if (d.n_group > 1) {
-      float my_gscore = -INFINITY;
-      for (int g = 0; g < d.n_group; ++g) {
-        float t1 = -INFINITY, t2 = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const int e = lane * EPL + i;
-          if (valid[i] && e / gs == g) {
-            float v = key[i];
-            if (v > t1) {
-              t2 = t1;
-              t1 = v;
-            } else if (v > t2) {
-              t2 = v;
-            }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
-          float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
-          float n1 = fmaxf(t1, o1);
-          t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
-          t1 = n1;
-        }
-        float sc = gs >= 2 ? __fadd_rn(t1, t2) : t1;
-        if (lane == g) my_gscore = sc;
-      }
-      kept = 0;
-      for (int r = 0; r < d.topk_group; ++r) {
-        bool cand = lane < d.n_group && !((kept >> lane) & 1u);
-        float v = cand ? my_gscore : -INFINITY;
-        int gi = cand ? lane : 64 + lane;
-        float dummy = 0.f;
-        warp_argmax(v, gi, dummy);
-        kept |= 1u << (gi & 31);
-      }
-    }
-
-    // expert stage
-    uint32_t taken = 0;
-    int sel_e = 0;
-    float sel_s = 0.f;
-    for (int j = 0; j < d.k; ++j) {
-      float bv = -INFINITY, bs = 0.f;
-      int be = 0x7fffffff;
+    int sel_e;
+    float sel_l;
+    bool clear;
+    select_experts<EPL>(d, key, lv, valid, lane, gs, sigmoid, sel_e, sel_l, clear);
+    if (sigmoid && !clear) {
+      // a near tie: decide on the exact keys
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const int e = lane * EPL + i;
-        const bool ok = valid[i] && !((taken >> i) & 1u) && ((kept >> (e / gs)) & 1u);
-        if (ok && (key[i] > bv || be == 0x7fffffff)) {
-          bv = key[i];
-          be = e;
-          bs = sv[i];
-        }
+        float kv = __fadd_rn(sigmoid_exact(lv[i]), bias[i]);
+        if (kv != kv) kv = -INFINITY;
+        key[i] = valid[i] ? kv : -INFINITY;
       }
-      warp_argmax(bv, be, bs);
-      if (be / EPL == lane) taken |= 1u << (be - lane * EPL);
-      if (lane == j) {
-        sel_e = be;
-        sel_s = bs;
-      }
+      select_experts<EPL>(d, key, lv, valid, lane, gs, false, sel_e, sel_l, clear);
     }
 
     // route weights
     double w = 0.0;
-    if (d.score == MOE_SCORE_SOFTMAX) {
+    if (!sigmoid) {
       float lmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (valid[i]) lmax = fmaxf(lmax, sv[i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+        if (valid[i]) lmax = fmaxf(lmax, lv[i]);
+      lmax = warp_max(lmax);
       double z = 0.0;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (valid[i]) z += exp((double)sv[i] - (double)lmax);
+        if (valid[i]) z += exp((double)lv[i] - (double)lmax);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (lane < d.k) w = exp((double)sel_s - (double)lmax) / z;
+      if (lane < d.k) w = exp((double)sel_l - (double)lmax) / z;
     } else {
-      if (lane < d.k) w = (double)sel_s;
+      if (lane < d.k) w = (double)sigmoid_exact(sel_l);
     }
     if (d.renorm) {
       double sum = lane < d.k ? w : 0.0;

@@ -281,3 +281,42 @@ def test_fp8_weight_quantiser_is_bit_exact():
         np.testing.assert_array_equal(q[b].cpu().numpy(), rq)
         np.testing.assert_array_equal(s[b].cpu().numpy(), rs)
     assert s[1, 0, 0].item() == 1.0
+
+
+@pytest.mark.parametrize("score", ["sigmoid", "softmax"])
+def test_routing_near_ties_bit_exact(score):
+    """Logits built to sit on decision boundaries (exact duplicates, neighbouring fp32 values, nearly
+    equal group scores) route exactly as the oracle routes them."""
+    rng = np.random.default_rng(21)
+    T, E, k = 4096, 256, 8
+    G, Gk = (8, 4) if score == "sigmoid" else (1, 1)
+    logits = rng.standard_normal((T, E)).astype(np.float32) * 2
+    for t in range(T):
+        kind = t % 4
+        a = rng.choice(E, 12, replace=False)
+        if kind == 0:  # exact duplicates around the selection boundary
+            logits[t, a] = logits[t, a[0]]
+        elif kind == 1:  # neighbouring fp32 values
+            v = np.float32(rng.uniform(0, 3))
+            for i, e in enumerate(a):
+                logits[t, e] = v
+                v = np.nextafter(v, np.float32(10))
+        elif kind == 2:  # two groups with nearly the same two best keys
+            g0, g1 = rng.choice(G, 2, replace=False) if G > 1 else (0, 0)
+            gsz = E // G
+            logits[t, g0 * gsz:g0 * gsz + 2] = 4.0
+            logits[t, g1 * gsz:g1 * gsz + 2] = np.nextafter(np.float32(4.0), np.float32(0))
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32) if score == "sigmoid" else None
+    wl = synth.WORKLOADS["dsv3_prefill"].replace(T=T, h=256, E=E, k=k, I=128, I_shared=0, n_group=G, topk_group=Gk,
+                                                 score=score, renorm=True)
+    cfg = cfg_of(wl)
+    lg = torch.from_numpy(logits).cuda()
+    b = None if bias is None else torch.from_numpy(bias).cuda()
+    dummy_w = torch.zeros(E, 256, dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    rde.route(cfg, None, rde.Weights(w_router=dummy_w, bias=b), idx, w, logits=lg, logits_given=True)
+    torch.cuda.synchronize()
+    ri, rw = oracle.route(logits, bias, **route_kwargs(wl))
+    np.testing.assert_array_equal(idx.cpu().numpy(), ri)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
