@@ -168,6 +168,22 @@ def time_cpu_oracle(wl, budget_s):
     return S / dt, S, dt
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (the job is as slow as its slowest replica)."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(world, tokens_per_replica, ms_per_step):
+    """Whole-job throughput of `world` independent replicas: all tokens over the slowest step time."""
+    return world * tokens_per_replica / (ms_per_step * 1e-3)
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -364,11 +380,7 @@ def main():
     torch.cuda.synchronize(dev)
     ms_e2e = e_s.elapsed_time(e_e) / e2e_steps
 
-    # max over ranks
-    vals = torch.tensor([ms_step, ms_e2e, gemm_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_step, ms_e2e, gemm_ms = vals.tolist()
+    ms_step, ms_e2e, gemm_ms = max_over_ranks([ms_step, ms_e2e, gemm_ms], dist, dev)
     status = rde.device_status(cfg, ws)
     if status != 0:
         raise SystemExit(f"device status {status} after the timed region")
@@ -397,7 +409,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * wl.T / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": job_tokens_per_s(world, wl.T, ms_step), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if wl.dtype == "fp8" else "bf16",
             "data": "synthetic", "config": config_of(wl, world),
@@ -413,7 +425,7 @@ def main():
                                "bound": "tensor" if t_compute >= bytes_ / p_hbm else "hbm",
                                "peaks": peaks_kind},
             "ms_moe_forward": ms_fwd, "ms_expert_ffn": gemm_ms,
-            "e2e": {"value": world * wl.T / (ms_e2e * 1e-3), "unit": UNIT,
+            "e2e": {"value": job_tokens_per_s(world, wl.T, ms_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                     "d2h_bytes_per_step": int(y.numel() * y.element_size())},
             "gpu_launches": int(n1 - n0),
