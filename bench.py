@@ -51,6 +51,14 @@ def layer_counts(wl, active_experts):
     return flops, gemm_flops, bytes_
 
 
+def gemm_source_sha():
+    """sha256 over the sources the grouped-GEMM kernels are compiled from."""
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "gemm_common.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "routing_dispatch_expert_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def gemm_traffic_from_profile(wl):
     """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it was taken on the
     current kernel source and this workload; else None."""
@@ -58,8 +66,7 @@ def gemm_traffic_from_profile(wl):
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    src = os.path.join(ROOT, "routing_dispatch_expert_gb300", "csrc", "gemm.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = gemm_source_sha()
     if d.get("kernel_source_sha256") != sha or d.get("workload") != wl.name:
         return None
     return d.get("dram_bytes_per_launch_full_size")

@@ -62,6 +62,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may be suspended by the hardware
+// until the phase completes or `sleep_ns` elapse, instead of returning at once (so waiting warps do
+// not spin on the barrier and take issue slots and shared-memory bandwidth from working warps).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t sleep_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(sleep_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up after `limit_cycles` SM clocks (then returns false). Every pipeline
 // wait in this library goes through here, so no kernel can spin forever.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit_cycles) {

@@ -93,13 +93,15 @@ __device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int 
   return t;
 }
 
+constexpr uint32_t kWaitSleepNs = 20000;  // one suspension of a waiting thread: at most 20 us
+
 // Bounded wait on an mbarrier phase. Gives up when another role of the CTA has aborted, or after
 // `limit` SM clocks (then it raises the CTA's abort flag and records MOE_STATUS_WAIT_TIMEOUT).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                               long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;
@@ -113,7 +115,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // Bounded drain used on the way out (normal or aborted): wait for a phase, give up after `limit`.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long limit) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity) && clock64() - t0 < limit) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs) && clock64() - t0 < limit) {
   }
 }
 
