@@ -59,6 +59,46 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   }
 }
 
+// k <= KMAX: all k (+1 shared) rows of a 256-element chunk are loaded before any is added, so a warp
+// keeps k + 1 independent 16-byte loads per lane in flight; the sum is still taken in slot order.
+template <int KMAX>
+__global__ void __launch_bounds__(256) combine_small_k_kernel(const uint4* __restrict__ yd,
+                                                              const int32_t* __restrict__ inv_pos,
+                                                              uint4* __restrict__ y, int T, int h, int k, int R,
+                                                              int shared) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int hv = h / 8;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const int my_row = lane < k ? inv_pos[(int64_t)t * k + lane] : -1;
+    int rows[KMAX + 1];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) rows[j] = __shfl_sync(0xffffffffu, my_row, j);  // -1 past k
+    rows[KMAX] = shared ? R + t : -1;
+    for (int c = lane; c < hv; c += 32) {
+      uint4 v[KMAX + 1];
+#pragma unroll
+      for (int j = 0; j <= KMAX; ++j)
+        v[j] = rows[j] >= 0 ? yd[(int64_t)rows[j] * hv + c] : make_uint4(0, 0, 0, 0);
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j <= KMAX; ++j) {
+        if (rows[j] < 0) continue;
+        const uint32_t a[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] += bf16_lo(a[i]);
+          acc[2 * i + 1] += bf16_hi(a[i]);
+        }
+      }
+      y[(int64_t)t * hv + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
 // one CTA per 128x128 tile: amax, scale = amax / 448 (1 if zero), codes rounded to nearest even
 __global__ void __launch_bounds__(256) quantize_weight_kernel(const uint4* __restrict__ w, int64_t rows, int64_t cols,
                                                               uint2* __restrict__ q, float* __restrict__ s) {
@@ -111,8 +151,13 @@ cudaError_t launch_combine(const void* yd, const int32_t* inv_pos, void* y, int 
   if (T == 0) return cudaSuccess;
   int64_t blocks = cdiv(T, 8);
   if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
-  cb::combine_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(yd), inv_pos,
-                                                            reinterpret_cast<uint4*>(y), T, h, k, T * k, shared);
+  if (k <= 8)
+    cb::combine_small_k_kernel<8><<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(yd), inv_pos,
+                                                                         reinterpret_cast<uint4*>(y), T, h, k, T * k,
+                                                                         shared);
+  else
+    cb::combine_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(yd), inv_pos,
+                                                              reinterpret_cast<uint4*>(y), T, h, k, T * k, shared);
   return cudaGetLastError();
 }
 
