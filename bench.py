@@ -371,6 +371,23 @@ def main():
     ms_fwd = fstart.elapsed_time(fend) / args.steps
     ms_step = ms_total / args.steps
 
+    # the same layer as one CUDA graph per step (moe_graph_*): launch cost removed
+    gstream = torch.cuda.Stream(dev)
+    gstream.wait_stream(stream)
+    with torch.cuda.stream(gstream):
+        graph = rde.Graph(cfg, x, weights, y, ws, gstream)
+        for _ in range(2):
+            graph.launch()
+        g_s, g_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gstream.synchronize()
+        g_s.record(gstream)
+        for _ in range(args.steps):
+            graph.launch()
+        g_e.record(gstream)
+    gstream.synchronize()
+    ms_graph = g_s.elapsed_time(g_e) / args.steps
+    del graph
+
     # end to end through the public API with host buffers: pinned x in, y out, every step
     x_host = x.cpu().pin_memory()
     y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
@@ -387,7 +404,7 @@ def main():
     torch.cuda.synchronize(dev)
     ms_e2e = e_s.elapsed_time(e_e) / e2e_steps
 
-    ms_step, ms_e2e, gemm_ms = max_over_ranks([ms_step, ms_e2e, gemm_ms], dist, dev)
+    ms_step, ms_e2e, gemm_ms, ms_graph = max_over_ranks([ms_step, ms_e2e, gemm_ms, ms_graph], dist, dev)
     status = rde.device_status(cfg, ws)
     if status != 0:
         raise SystemExit(f"device status {status} after the timed region")
@@ -432,6 +449,8 @@ def main():
                                "bound": "tensor" if t_compute >= bytes_ / p_hbm else "hbm",
                                "peaks": peaks_kind},
             "ms_moe_forward": ms_fwd, "ms_expert_ffn": gemm_ms,
+            "graph": {"value": job_tokens_per_s(world, wl.T, ms_graph), "unit": UNIT, "ms_per_step": ms_graph,
+                      "note": "the same step replayed as one CUDA graph (moe_graph_launch)"},
             "e2e": {"value": job_tokens_per_s(world, wl.T, ms_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": int(x.numel() * x.element_size()),
                     "d2h_bytes_per_step": int(y.numel() * y.element_size())},

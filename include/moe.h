@@ -207,6 +207,20 @@ int moe_combine(const moe_config* cfg, const void* yd, const int32_t* inv_pos, v
 int moe_forward(const moe_config* cfg, const void* x, const moe_weights* weights, void* y, void* ws,
                 size_t ws_bytes, moe_stream_t stream);
 
+/* The whole layer as one CUDA graph (Perplexity "CUDA Graph": one graph per batch size removes the
+ * per-kernel launch cost; TensorRT-LLM "Runtime optimizations": CUDA graphs with padding to the
+ * nearest captured size). moe_graph_create runs moe_forward once eagerly (lazy set-up), then captures
+ * moe_forward(cfg, x, weights, y, ws) on `stream` and instantiates it. The graph keeps every pointer:
+ * each moe_graph_launch recomputes y from whatever x holds at that time, with the same config.
+ * `stream` must not be the legacy default stream. The caller keeps x, y, ws and the weights alive
+ * and unmoved until moe_graph_destroy. Launches on one graph must not overlap (shared workspace).
+ * Errors: as moe_forward; MOE_ERR_CUDA if capture or instantiation fails. */
+typedef struct moe_graph_s* moe_graph;
+int moe_graph_create(const moe_config* cfg, const void* x, const moe_weights* weights, void* y, void* ws,
+                     size_t ws_bytes, moe_stream_t stream, moe_graph* graph);
+int moe_graph_launch(moe_graph graph, moe_stream_t stream);
+int moe_graph_destroy(moe_graph graph);
+
 /* Static 128x128 weight quantisation for the FP8 layer (Perplexity "Quantization": weights are
  * quantised statically per 128x128 tile). For each of `batch` row-major [rows, cols] bf16
  * matrices: scale = amax(tile) / 448 (1 for an all-zero tile), code = e4m3(w / scale) rounded to

@@ -439,6 +439,66 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   return MOE_OK;
 }
 
+// ------------------------------------------------------------------------------------------
+// CUDA graph of the whole layer
+// ------------------------------------------------------------------------------------------
+struct moe_graph_s {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int kernels = 0;  // library kernels per launch
+};
+
+MOE_EXPORT int moe_graph_create(const moe_config* cfg, const void* x, const moe_weights* weights, void* y, void* ws,
+                                size_t ws_bytes, moe_stream_t stream, moe_graph* graph) {
+  if (!graph) return fail(MOE_ERR_INVALID, "graph is NULL");
+  *graph = nullptr;
+  if (!stream) return fail(MOE_ERR_INVALID, "capture needs a created stream, not the legacy default stream");
+  cudaStream_t s = (cudaStream_t)stream;
+  // eager run: validates the arguments and performs the lazy one-time set-up outside the capture
+  int rc = moe_forward(cfg, x, weights, y, ws, ws_bytes, stream);
+  if (rc) return rc;
+  const uint64_t before = g_launches.load();
+  cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
+  rc = moe_forward(cfg, x, weights, y, ws, ws_bytes, stream);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(s, &g);
+  if (rc) {
+    if (g) cudaGraphDestroy(g);
+    return rc;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  moe_graph_s* out = new moe_graph_s;
+  out->graph = g;
+  out->exec = ex;
+  out->kernels = (int)(g_launches.load() - before);
+  g_launches.fetch_sub((uint64_t)out->kernels);  // captured, not launched
+  *graph = out;
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_graph_launch(moe_graph graph, moe_stream_t stream) {
+  if (!graph) return fail(MOE_ERR_INVALID, "graph is NULL");
+  cudaError_t e = cudaGraphLaunch(graph->exec, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+  counted(graph->kernels);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_graph_destroy(moe_graph graph) {
+  if (!graph) return MOE_OK;
+  if (graph->exec) cudaGraphExecDestroy(graph->exec);
+  if (graph->graph) cudaGraphDestroy(graph->graph);
+  delete graph;
+  return MOE_OK;
+}
+
 MOE_EXPORT int moe_quantize_weights_fp8(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, float* s,
                                         moe_stream_t stream) {
   if (batch < 0 || rows < 0 || cols < 0) return fail(MOE_ERR_INVALID, "negative size");

@@ -72,6 +72,9 @@ def load():
                 "moe_forward": [cfgp, vp, wp, vp, vp, sz, vp],
                 "moe_quantize_weights_fp8": [vp, i64, i64, i64, vp, vp, vp],
                 "moe_device_status": [cfgp, vp, ctypes.POINTER(ctypes.c_int32), vp],
+                "moe_graph_create": [cfgp, vp, wp, vp, vp, sz, vp, ctypes.POINTER(vp)],
+                "moe_graph_launch": [vp, vp],
+                "moe_graph_destroy": [vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -215,3 +218,64 @@ class MoeLayer:
             y = torch.empty_like(x)
         forward(self.cfg, x, self.weights, y, self.ws)
         return y
+
+
+class Graph:
+    """moe_forward captured as one CUDA graph (moe_graph_create); launch() recomputes y from x."""
+
+    def __init__(self, cfg, x, weights: Weights, y, ws, stream=None):
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        if self.stream.cuda_stream == 0:
+            raise ValueError("capture needs a created CUDA stream, not the legacy default stream")
+        self._keep = (cfg, x, weights, y, ws)
+        h = ctypes.c_void_p()
+        _check(load().moe_graph_create(ctypes.byref(cfg), _ptr(x), ctypes.byref(weights.struct), _ptr(y), _ptr(ws),
+                                       ws.numel(), ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h)))
+        self._h = h
+
+    def launch(self):
+        _check(load().moe_graph_launch(self._h, ctypes.c_void_p(self.stream.cuda_stream)))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            load().moe_graph_destroy(h)
+
+
+class GraphedMoeLayer:
+    """One CUDA graph per padded batch size (the nearest captured size at or above the batch). The graphs
+    share static x / y buffers and one workspace sized for the largest batch; padding rows are computed
+    and dropped (every token's output depends only on its own row)."""
+
+    def __init__(self, make_cfg, weights: Weights, sizes, h, device="cuda", stream=None):
+        self.sizes = sorted(set(int(t) for t in sizes))
+        self.weights = weights
+        self.stream = stream if stream is not None else torch.cuda.Stream(device=device)
+        t_max = self.sizes[-1]
+        self.x = torch.zeros(t_max, h, dtype=torch.bfloat16, device=device)
+        self.y = torch.zeros(t_max, h, dtype=torch.bfloat16, device=device)
+        self.ws = alloc_workspace(make_cfg(t_max), device)
+        self.graphs = {}
+        with torch.cuda.stream(self.stream):
+            device_status(make_cfg(t_max), self.ws)
+            for t in self.sizes:
+                cfg = make_cfg(t)
+                self.graphs[t] = Graph(cfg, self.x[:t], weights, self.y[:t], self.ws, self.stream)
+        self.stream.synchronize()
+
+    def padded_size(self, T: int) -> int:
+        for t in self.sizes:
+            if t >= T:
+                return t
+        raise ValueError(f"batch of {T} tokens exceeds the largest captured size {self.sizes[-1]}")
+
+    def __call__(self, x: torch.Tensor) -> torch.Tensor:
+        T = x.shape[0]
+        t = self.padded_size(T)
+        self.stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.stream):
+            self.x[:T].copy_(x)
+            self.graphs[t].launch()
+            out = self.y[:T].clone()
+        torch.cuda.current_stream().wait_stream(self.stream)
+        return out
