@@ -77,6 +77,10 @@ typedef struct {
   int32_t renormalize;  /* 1: divide the selected weights by their sum */
   float routed_scale;   /* multiplies the routed weights (DeepSeek-V3: 2.5) */
   int32_t dtype;        /* MOE_DTYPE_BF16 | MOE_DTYPE_FP8_BLOCK128 */
+  float capacity_factor;/* 0: dropless. > 0: every expert keeps at most ceil(capacity_factor * T * k / E)
+                           assignments, the earliest tokens first; the rest skip that expert (Ultralytics
+                           "Load balancing and capacity": a capacity factor such as 1.25x the fair
+                           share; skipped tokens pass through the residual connection) */
 } moe_config;
 
 typedef struct {
@@ -143,8 +147,8 @@ int moe_route(const moe_config* cfg, const void* x, const moe_weights* weights, 
  * each token's hidden state is copied k times). Dropless.
  *   x          [T, h] bf16
  *   topk_idx   [T, k] int32, topk_w [T, k] fp32 (from moe_route)
- *   counts     [E] int32 out: rows per expert
- *   offsets    [E + 1] int32 out: exclusive prefix of counts (offsets[E] = T*k)
+ *   counts     [E] int32 out: rows per expert (at most the capacity when capacity_factor > 0)
+ *   offsets    [E + 1] int32 out: exclusive prefix of counts (offsets[E] = T*k when dropless)
  *   inv_pos    [T, k] int32 out: expert-major row of (token, slot); within an expert rows are in
  *              ascending token order
  *   row_token  [T*k] int32 out: token of each row;  row_weight [T*k] fp32 out: its route weight
@@ -153,7 +157,8 @@ int moe_route(const moe_config* cfg, const void* x, const moe_weights* weights, 
  *              block (Perplexity "Quantization": activations scaled per 128-element vector at
  *              run time) with xd_scales [R_tot, h/128] fp32 (NULL for bf16)
  *   ws         workspace (scratch histograms and the device status word)
- * A topk_idx entry outside [0, E) is skipped and sets MOE_STATUS_BAD_EXPERT_INDEX.
+ * A topk_idx entry outside [0, E) is skipped and sets MOE_STATUS_BAD_EXPERT_INDEX. An assignment
+ * beyond an expert's capacity is dropped: its inv_pos is -1, it has no row, and combine leaves it out.
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA. */
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_w,
                  int32_t* counts, int32_t* offsets, int32_t* inv_pos, int32_t* row_token, float* row_weight,

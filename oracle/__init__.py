@@ -49,6 +49,8 @@ def lib():
             L.orc_permute.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp]
             L.orc_permute.restype = i32
             L.orc_gather_rows.argtypes = [vp, i64, i32, vp, i64, vp]
+            L.orc_permute_capacity.argtypes = [vp, i64, i32, i32, i32, vp, vp, vp, vp]
+            L.orc_permute_capacity.restype = i32
             L.orc_expert_ffn_bf16.argtypes = [vp, i64, i64, i64, vp, vp, vp]
             L.orc_expert_ffn_fp8.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, vp]
             L.orc_combine.argtypes = [vp, vp, vp, i64, i32, i64, vp]
@@ -160,6 +162,29 @@ def permute(topk_idx, E):
     return counts, offsets, inv_pos, row_token
 
 
+def capacity(capacity_factor, T, k, E) -> int:
+    """Assignments an expert may keep: ceil(capacity_factor * T * k / E); 0 = no limit."""
+    if capacity_factor <= 0:
+        return 0
+    import math
+    return int(math.ceil(capacity_factor * T * k / E))
+
+
+def permute_capacity(topk_idx, E, cap):
+    """permute() with at most `cap` rows per expert (earliest tokens); dropped entries get inv_pos -1.
+    Returns (counts, offsets, inv_pos, row_token[:offsets[E]])."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    inv_pos = np.empty((T, k), np.int32)
+    row_token = np.empty(T * k, np.int32)
+    if lib().orc_permute_capacity(_p(idx), T, k, E, int(cap), _p(counts), _p(offsets), _p(inv_pos),
+                                  _p(row_token)) != 0:
+        raise ValueError("expert index out of range")
+    return counts, offsets, inv_pos, row_token[:offsets[E]]
+
+
 def gather_rows(x, row_token) -> np.ndarray:
     x = np.ascontiguousarray(x)
     rt = _c(row_token, np.int32)
@@ -218,7 +243,7 @@ def imbalance(counts, n_cards) -> float:
 
 # ---------------------------------------------------------------- whole layer (small shapes)
 def forward(x_bf16, w_r, bias, experts, shared, *, k, n_group=1, topk_group=1, score=SOFTMAX, renorm=False,
-            routed_scale=1.0, fp8=False, logits=None):
+            routed_scale=1.0, fp8=False, logits=None, capacity_factor=0.0):
     """The whole layer for shapes the oracle finishes in seconds.
 
     experts: list of (w_gu [2I, h], w_d [h, I]) bf16 per routed expert; shared: same tuple or None.
@@ -232,8 +257,12 @@ def forward(x_bf16, w_r, bias, experts, shared, *, k, n_group=1, topk_group=1, s
     if logits is None:
         logits = router_logits(x, w_r)
     idx, w = route(logits, bias, k, n_group, topk_group, score, renorm, routed_scale)
-    counts, offsets, inv_pos, row_token = permute(idx, E)
-    R = T * k
+    cap = capacity(capacity_factor, T, k, E)
+    if cap > 0:
+        counts, offsets, inv_pos, row_token = permute_capacity(idx, E, cap)
+    else:
+        counts, offsets, inv_pos, row_token = permute(idx, E)
+    R = int(offsets[E])
     out = dict(logits=logits, topk_idx=idx, topk_w=w, counts=counts, offsets=offsets, inv_pos=inv_pos,
                row_token=row_token)
     if fp8:
@@ -258,6 +287,8 @@ def forward(x_bf16, w_r, bias, experts, shared, *, k, n_group=1, topk_group=1, s
             a, b = offsets[e], offsets[e + 1]
             o_rows[a:b] = expert_ffn_bf16(xd[a:b], experts[e][0], experts[e][1])
         sh = None if shared is None else expert_ffn_bf16(x, shared[0], shared[1])
-    o = o_rows[inv_pos.reshape(-1)].reshape(T, k, h)
+    # a dropped (token, slot) (inv_pos -1) contributes nothing: its expert output is zero
+    flat = inv_pos.reshape(-1)
+    o = np.where((flat >= 0)[:, None], o_rows[np.maximum(flat, 0)] if R > 0 else 0.0, 0.0).reshape(T, k, h)
     out.update(o_rows=o_rows, shared_out=sh, y=combine(o, w, sh))
     return out

@@ -316,6 +316,39 @@ ORC_API int orc_permute(const int32_t* topk_idx, int64_t T, int k, int E, int32_
   return 0;
 }
 
+/* Capacity limit ([ULTRA] "Load balancing and capacity": each expert accepts at most a fixed number
+ * of assignments per batch, e.g. 1.25 times the fair share; the rest skip the expert). The expert keeps
+ * its earliest `cap` tokens (ascending token order); a dropped (token, slot) gets inv_pos = -1 and no
+ * row. cap <= 0 means no limit. */
+ORC_API int orc_permute_capacity(const int32_t* topk_idx, int64_t T, int k, int E, int32_t cap, int32_t* counts,
+                                 int32_t* offsets, int32_t* inv_pos, int32_t* row_token) {
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t i = 0; i < T * k; ++i) {
+    if (topk_idx[i] < 0 || topk_idx[i] >= E) return -1;
+    inv_pos[i] = -1;
+  }
+  for (int e = 0; e < E; ++e) {
+    int32_t taken = 0;
+    for (int64_t t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j)
+        if (topk_idx[t * k + j] == e && (cap <= 0 || taken < cap)) taken++;
+    counts[e] = taken;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  for (int e = 0; e < E; ++e) {
+    int32_t r = 0;
+    for (int64_t t = 0; t < T && r < counts[e]; ++t)
+      for (int j = 0; j < k; ++j)
+        if (topk_idx[t * k + j] == e) {
+          int32_t row = offsets[e] + r++;
+          row_token[row] = (int32_t)t;
+          inv_pos[t * k + j] = row;
+        }
+  }
+  return 0;
+}
+
 /* Dispatch copy ([INFRA] 3.1 step 2: the hidden state of each token is copied once per
  * chosen expert): xd[row] = x[row_token[row]]. Element type of width `elem` bytes. */
 ORC_API void orc_gather_rows(const void* x, int64_t h, int elem, const int32_t* row_token, int64_t R, void* xd) {

@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -50,6 +51,7 @@ int check_config(const moe_config* c) {
   if (c->I % 128 != 0) return fail(MOE_ERR_UNSUPPORTED, "I must be a multiple of 128");
   if (c->I_shared != 0 && c->I_shared != c->I) return fail(MOE_ERR_UNSUPPORTED, "I_shared must be 0 or I");
   if ((int64_t)c->T * (c->k + 1) > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "T * (k + 1) exceeds int32 rows");
+  if (!(c->capacity_factor >= 0.f)) return fail(MOE_ERR_INVALID, "capacity_factor must be >= 0");
   return MOE_OK;
 }
 
@@ -176,6 +178,13 @@ int do_route(const moe_config* c, const void* x, const moe_weights* w, float* lo
   return MOE_OK;
 }
 
+// ceil(capacity_factor * T * k / E) assignments per expert, 0 = no limit
+int capacity_of(const moe_config* c) {
+  if (c->capacity_factor <= 0.f) return 0;
+  const double cap = std::ceil((double)c->capacity_factor * (double)c->T * c->k / c->E);
+  return cap >= (double)INT32_MAX ? 0 : (int)cap;
+}
+
 int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, const float* topk_w, int32_t* counts,
                 int32_t* offsets, int32_t* inv_pos, int32_t* row_token, float* row_weight, void* xd, float* xd_scales,
                 void* ws, const Layout& L, cudaStream_t stream) {
@@ -198,6 +207,7 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   d.k = c->k;
   d.shared = c->I_shared > 0;
   d.fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
+  d.capacity = capacity_of(c);
   cudaError_t e = moe::launch_dispatch(d, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   if (c->T > 0) counted(4);
@@ -618,6 +628,7 @@ MOE_EXPORT int moe_dispatch_noalloc(const moe_config* cfg, const void* x, const 
   d.k = cfg->k;
   d.shared = cfg->I_shared > 0;
   d.fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+  d.capacity = capacity_of(cfg);
   e = moe::launch_dispatch(d, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   if (cfg->T > 0) counted(4);

@@ -8,7 +8,8 @@
 // Four kernels, all deterministic (integer atomics only, whose results do not depend on order):
 //   1. histogram   per 512-token block: counts of each expert      -> hist[block][E]
 //   2. scan        one CTA: per-expert running sum over blocks, exclusive scan over experts
-//                  -> counts, offsets, and the first row of every (block, expert)
+//                  -> counts (clamped to the capacity), offsets, and the within-expert rank of every
+//                  (block, expert)
 //   3. rank        per 512-token block: per-warp lane masks of each expert give every (token, slot)
 //                  its row, rows of an expert in ascending token order -> inv_pos, row_token,
 //                  row_weight
@@ -46,7 +47,9 @@ __global__ void __launch_bounds__(TPB) hist_kernel(const int32_t* __restrict__ i
   for (int e = threadIdx.x; e < E; e += TPB) hist[(int64_t)blockIdx.x * E + e] = sh[e];
 }
 
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nblk, int E,
+// hist[b][e] becomes the number of earlier tokens (blocks < b) that chose e, i.e. the rank within
+// expert e of block b's first such token; counts are clamped to the capacity `cap`.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nblk, int E, int cap,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   __shared__ int32_t warp_tot[32];
   const int e = threadIdx.x;  // E <= 1024
@@ -57,6 +60,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
       hist[(int64_t)b * E + e] = run;
       run += c;
     }
+    run = min(run, cap);
     counts[e] = run;
   }
   // exclusive scan of run over experts
@@ -83,15 +87,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
   const int excl = warp_tot[w] + incl - run;
   if (e < E) offsets[e] = excl;
   if (e == E - 1) offsets[E] = excl + run;
-  __syncthreads();
-  if (e < E)
-    for (int b = 0; b < nblk; ++b) hist[(int64_t)b * E + e] += excl;
 }
 
 __global__ void __launch_bounds__(TPB) rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
-                                                   const int32_t* __restrict__ base, int T, int k, int E,
-                                                   int32_t* __restrict__ inv_pos, int32_t* __restrict__ row_token,
-                                                   float* __restrict__ row_weight) {
+                                                   const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
+                                                   int T, int k, int E, int cap, int32_t* __restrict__ inv_pos,
+                                                   int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
   extern __shared__ uint32_t smem[];
   uint32_t* masks = smem;                                        // [WARPS][E]
   int32_t* wbase = reinterpret_cast<int32_t*>(smem + WARPS * E);  // [WARPS][E]
@@ -120,9 +121,12 @@ __global__ void __launch_bounds__(TPB) rank_kernel(const int32_t* __restrict__ i
       int e = idx[t * k + j];
       int row = -1;
       if (e >= 0 && e < E) {
-        row = wbase[w * E + e] + __popc(masks[w * E + e] & lt);
-        row_token[row] = (int32_t)t;
-        row_weight[row] = topk_w[t * k + j];
+        const int rank = wbase[w * E + e] + __popc(masks[w * E + e] & lt);  // earlier tokens choosing e
+        if (rank < cap) {
+          row = offsets[e] + rank;
+          row_token[row] = (int32_t)t;
+          row_weight[row] = topk_w[t * k + j];
+        }
       }
       inv_pos[t * k + j] = row;
     }
@@ -223,7 +227,8 @@ cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
   }
   const int nblk = dispatch_blocks(d.T);
   dp::hist_kernel<<<nblk, dp::TPB, sizeof(int32_t) * d.E, stream>>>(d.topk_idx, d.T, d.k, d.E, d.scratch, d.status);
-  dp::scan_kernel<<<1, 1024, 0, stream>>>(d.scratch, nblk, d.E, d.counts, d.offsets);
+  const int cap = d.capacity > 0 ? d.capacity : 0x7fffffff;
+  dp::scan_kernel<<<1, 1024, 0, stream>>>(d.scratch, nblk, d.E, cap, d.counts, d.offsets);
   const size_t rank_smem = sizeof(uint32_t) * 2 * dp::WARPS * d.E;
   static bool attr = false;
   if (!attr) {
@@ -232,8 +237,8 @@ cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dp::rank_kernel<<<nblk, dp::TPB, rank_smem, stream>>>(d.topk_idx, d.topk_w, d.scratch, d.T, d.k, d.E, d.inv_pos,
-                                                         d.row_token, d.row_weight);
+  dp::rank_kernel<<<nblk, dp::TPB, rank_smem, stream>>>(d.topk_idx, d.topk_w, d.scratch, d.offsets, d.T, d.k, d.E,
+                                                         cap, d.inv_pos, d.row_token, d.row_weight);
   int64_t blocks = cdiv(d.T, 8);
   if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
   const int R = d.T * d.k;

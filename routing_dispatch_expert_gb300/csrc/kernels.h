@@ -48,6 +48,7 @@ struct DispatchDesc {
   int T, h, E, k;
   int shared;  // also write the T token rows for the shared expert
   int fp8;
+  int capacity = 0;  // > 0: keep at most this many rows per expert (earliest tokens)
 };
 cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream);
 

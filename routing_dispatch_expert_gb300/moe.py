@@ -32,7 +32,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("h", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("score", ctypes.c_int32), ("renormalize", ctypes.c_int32),
-                ("routed_scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+                ("routed_scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("capacity_factor", ctypes.c_float)]
 
 
 class MoeWeightsStruct(ctypes.Structure):
@@ -102,10 +102,11 @@ def _stream():
 
 
 def make_config(T, h, E, k, I, I_shared=0, n_group=1, topk_group=1, score="softmax", renorm=False, routed_scale=1.0,
-                dtype="bf16") -> MoeConfig:
+                dtype="bf16", capacity_factor=0.0) -> MoeConfig:
     return MoeConfig(T, h, E, k, I, I_shared, n_group, topk_group,
                      MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID, int(bool(renorm)),
-                     float(routed_scale), MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP8_BLOCK128)
+                     float(routed_scale), MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP8_BLOCK128,
+                     float(capacity_factor))
 
 
 class Weights:

@@ -51,6 +51,7 @@ class Workload:
     x_sigma: float = 1.0
     w_sigma: float = 0.02
     wr_sigma: float = 0.02
+    capacity_factor: float = 0.0  # 0: dropless
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

@@ -17,7 +17,7 @@ MARGIN = 1e-3  # tokens whose selection margin is below this are excluded when r
 def cfg_of(wl: synth.Workload) -> rde.MoeConfig:
     return rde.make_config(T=wl.T, h=wl.h, E=wl.E, k=wl.k, I=wl.I, I_shared=wl.I_shared, n_group=wl.n_group,
                            topk_group=wl.topk_group, score=wl.score, renorm=wl.renorm, routed_scale=wl.routed_scale,
-                           dtype=wl.dtype)
+                           dtype=wl.dtype, capacity_factor=wl.capacity_factor)
 
 
 def route_kwargs(wl: synth.Workload) -> dict:

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_sizes_match_header_layout():
-    assert ctypes.sizeof(moe.MoeConfig) == 12 * 4
+    assert ctypes.sizeof(moe.MoeConfig) == 13 * 4
     assert ctypes.sizeof(moe.MoeWeightsStruct) == 10 * 8
     assert ctypes.sizeof(moe.MoeWsLayout) == 16 * 8
 

@@ -30,6 +30,11 @@ SMALL = {
     "fp8_small": _W["dsv3_fp8"].replace(name="fp8_small", T=300, h=512, E=64, I=256, I_shared=256),
     "fp8_e256_skew": _W["dsv3_fp8"].replace(name="fp8_e256_skew", T=257, h=256, E=256, I=128, I_shared=128),
     "fp8_noshared": _W["dsv3_fp8"].replace(name="fp8_noshared", T=129, h=512, E=32, I=384, I_shared=0),
+    # capacity factor: overflowing experts keep their earliest tokens, the rest skip them
+    "cap_skew": _W["dsv3_decode"].replace(name="cap_skew", T=300, h=512, E=64, I=256, I_shared=256,
+                                          capacity_factor=1.25),
+    "cap_mixtral": _W["mixtral"].replace(name="cap_mixtral", T=500, h=512, I=256, capacity_factor=1.0),
+    "cap_fp8": _W["dsv3_fp8"].replace(name="cap_fp8", T=200, h=256, E=32, I=128, I_shared=128, capacity_factor=1.1),
 }
 
 
@@ -64,36 +69,39 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
     assert np.all(np.abs(logits.astype(np.float64) - lo) <= logit_tolerance(x, w_r))
 
     # the whole layer on identical logits
-    ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, fp8=wl.dtype == "fp8", **route_kwargs(wl))
+    ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, fp8=wl.dtype == "fp8",
+                         capacity_factor=wl.capacity_factor, **route_kwargs(wl))
     np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), ref["topk_idx"])
     np.testing.assert_allclose(it["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-6, atol=1e-7)
     np.testing.assert_array_equal(it["counts"].cpu().numpy(), ref["counts"])
     np.testing.assert_array_equal(it["offsets"].cpu().numpy(), ref["offsets"])
     np.testing.assert_array_equal(it["inv_pos"].cpu().numpy(), ref["inv_pos"])
-    np.testing.assert_array_equal(it["row_token"].cpu().numpy(), ref["row_token"])
+    Rk = int(ref["offsets"][-1])  # kept routed rows (T*k when dropless)
+    np.testing.assert_array_equal(it["row_token"].cpu().numpy()[:Rk], ref["row_token"][:Rk])
     rw = it["row_weight"].cpu().numpy()
-    np.testing.assert_array_equal(rw[ref["inv_pos"].ravel()], it["topk_w"].cpu().numpy().ravel())
+    kept = ref["inv_pos"].ravel() >= 0
+    np.testing.assert_array_equal(rw[ref["inv_pos"].ravel()[kept]], it["topk_w"].cpu().numpy().ravel()[kept])
     R = wl.T * wl.k
     fp8 = wl.dtype == "fp8"
     tol = FP8_TOL if fp8 else BF16_TOL
     if fp8:  # codes and 1x128 scales of the dispatched rows are decided identically: bit-exact
         xd = it["xd"].cpu().numpy()
         xs = it["xd_scales"].cpu().numpy()
-        np.testing.assert_array_equal(xd[:R], ref["xd"])
-        np.testing.assert_array_equal(xs[:R], ref["xd_scales"])
+        np.testing.assert_array_equal(xd[:Rk], ref["xd"])
+        np.testing.assert_array_equal(xs[:Rk], ref["xd_scales"])
         if wl.has_shared:
             np.testing.assert_array_equal(xd[R:], ref["xq"])
             np.testing.assert_array_equal(xs[R:], ref["xs"])
     else:
         xd = bits(it["xd"])
-        np.testing.assert_array_equal(xd[:R], ref["xd"])
+        np.testing.assert_array_equal(xd[:Rk], ref["xd"])
         if wl.has_shared:
             np.testing.assert_array_equal(xd[R:], x)
 
     # expert outputs per row (route-weighted), and the shared expert's rows
     yd = oracle.bf16_to_double(bits(it["yd"]))
-    o_w = ref["o_rows"] * rw[:, None].astype(np.float64)
-    err = np.abs(yd[:R] - o_w).max(axis=1) / np.maximum(np.abs(o_w).max(axis=1), 1e-30)
+    o_w = ref["o_rows"] * rw[:Rk, None].astype(np.float64)
+    err = np.abs(yd[:Rk] - o_w).max(axis=1) / np.maximum(np.abs(o_w).max(axis=1), 1e-30)
     assert err.max() <= tol, f"routed rows: max rel err {err.max()}"
     if wl.has_shared:
         s = ref["shared_out"]

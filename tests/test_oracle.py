@@ -374,3 +374,35 @@ def test_p5_imbalance_table():
     assert sum(c) / len(c) == g["average"]
     for ep, val in g["contiguous_imbalance"].items():
         assert round(oracle.imbalance(c, int(ep)), 2) == pytest.approx(val)
+
+
+# ------------------------------------------------------------------------------------ capacity
+def test_capacity_keeps_the_earliest_tokens():
+    rng = np.random.default_rng(15)
+    T, E, k = 300, 8, 2
+    pop = np.array([8, 4, 2, 1, 1, 1, 1, 1], np.float64)
+    idx = np.stack([rng.choice(E, k, replace=False, p=pop / pop.sum()) for _ in range(T)]).astype(np.int32)
+    cap = oracle.capacity(1.25, T, k, E)
+    assert cap == int(np.ceil(1.25 * T * k / E))
+    counts, offsets, inv_pos, row_token = oracle.permute_capacity(idx, E, cap)
+    full = np.bincount(idx.ravel(), minlength=E)
+    np.testing.assert_array_equal(counts, np.minimum(full, cap))
+    assert full.max() > cap  # the skew really overflows some expert
+    for e in range(E):
+        toks = np.nonzero((idx == e).any(axis=1))[0]  # tokens choosing e, ascending
+        kept = toks[:cap]
+        np.testing.assert_array_equal(row_token[offsets[e]:offsets[e + 1]], kept)
+        for t in toks[cap:]:
+            assert inv_pos[t, list(idx[t]).index(e)] == -1
+    # rows of kept entries point back at their token
+    ok = inv_pos >= 0
+    np.testing.assert_array_equal(row_token[inv_pos[ok]], np.nonzero(ok)[0])
+
+
+def test_capacity_above_the_largest_load_is_dropless():
+    rng = np.random.default_rng(16)
+    idx = np.stack([rng.choice(16, 4, replace=False) for _ in range(200)]).astype(np.int32)
+    a = oracle.permute(idx, 16)
+    b = oracle.permute_capacity(idx, 16, 10 ** 6)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
