@@ -64,6 +64,20 @@ typedef struct CUstream_st* moe_stream_t; /* the same handle type as cudaStream_
 #define MOE_STATUS_BAD_EXPERT_INDEX 1 /* a topk_idx entry outside [0, E) was skipped */
 #define MOE_STATUS_WAIT_TIMEOUT 2     /* a pipeline wait gave up; outputs of that call are invalid */
 
+/* Physical expert slots of a placement with redundant replicas (inference guide 6.4, sections 5.2-5.3,
+ * EPLB). Device arrays. Slot s serves logical expert slot_expert[s] as its replica slot_replica[s];
+ * replica i of expert e sits in slot replica_slot[e * max_replicas + i]. An expert's assignments go
+ * round-robin over its replicas in token order: the r-th kept token of expert e goes to replica
+ * r % replicas[e], row r / replicas[e] of that slot. moe_eplb_plan fills these tables. */
+typedef struct {
+  int32_t n_slots;              /* E + redundant replicas; at most 1024 */
+  int32_t max_replicas;         /* row length of replica_slot */
+  const int32_t* slot_expert;   /* [n_slots] */
+  const int32_t* slot_replica;  /* [n_slots] */
+  const int32_t* replicas;      /* [E] */
+  const int32_t* replica_slot;  /* [E, max_replicas] */
+} moe_placement;
+
 typedef struct {
   int32_t T;            /* tokens */
   int32_t h;            /* hidden size */
@@ -81,6 +95,8 @@ typedef struct {
                            assignments, the earliest tokens first; the rest skip that expert (Ultralytics
                            "Load balancing and capacity": a capacity factor such as 1.25x the fair
                            share; skipped tokens pass through the residual connection) */
+  const moe_placement* placement; /* NULL: one slot per expert. Otherwise the expert-major buffers,
+                           counts and offsets are per physical slot (n_slots of them) in slot order */
 } moe_config;
 
 typedef struct {
@@ -171,8 +187,8 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, 
  * (cudaMalloc may also synchronise the whole device, which such callers cannot afford).
  * Its scratch (per-block histograms, 512 KiB) is a static array in the library's own device memory,
  * held by every GPU that loads the library until the process exits. Limits and behaviour:
- *   - ceil(T / 512) * E must not exceed 131072 (e.g. E = 256 allows T up to 262144); larger sizes
- *     return MOE_ERR_UNSUPPORTED before any work is enqueued;
+ *   - (ceil(T / 512) + 1) * E must not exceed 131072 (e.g. E = 256 allows T up to 261632); larger
+ *     sizes return MOE_ERR_UNSUPPORTED before any work is enqueued;
  *   - allocates nothing: no cudaMalloc / cudaFree / allocating library routine;
  *   - the first call on a device looks up the array's device address on that device (set-up), so
  *     make that first call before any stream capture;
@@ -234,6 +250,19 @@ int moe_graph_destroy(moe_graph graph);
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 int moe_quantize_weights_fp8(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, float* s,
                              moe_stream_t stream);
+
+/* EPLB placement plan (inference guide 6.4, sections 5.2-5.3), on the host: n_redundant extra replicas
+ * go one by one to the expert with the largest load per replica (first expert on ties); then every
+ * replica, carrying load / replicas, is placed heaviest first (expert order on ties) onto the card with
+ * the smallest load that still has a free slot (first card on ties). n_cards cards of
+ * (E + n_redundant) / n_cards slots each, card-major slot numbering.
+ *   load [E] host in: assignments per expert (e.g. counts of recent steps)
+ *   replicas [E], slot_expert [E + n_redundant], slot_replica [E + n_redundant],
+ *   replica_slot [E * (n_redundant + 1)] (max_replicas = n_redundant + 1; unused entries -1),
+ *   card_load [n_cards] (sum of load / replicas on each card) -- host out.
+ * Errors: MOE_ERR_INVALID ((E + n_redundant) % n_cards != 0, NULL). */
+int moe_eplb_plan(const int64_t* load, int32_t E, int32_t n_cards, int32_t n_redundant, int32_t* replicas,
+                  int32_t* slot_expert, int32_t* slot_replica, int32_t* replica_slot, double* card_load);
 
 /* Device status word of a workspace: waits for `stream`, then reads the MOE_STATUS_* bits that
  * kernels of earlier calls with this workspace set into *status, and clears them. moe_forward clears

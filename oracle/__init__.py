@@ -231,7 +231,77 @@ def combine(o, w, shared=None) -> np.ndarray:
     return y
 
 
+# ---------------------------------------------------------------- expert placement
+def eplb_plan(load, n_cards, n_redundant):
+    """EPLB placement (inference guide 6.4, sections 5.2-5.3), the definition step by step:
+    1. each of the n_redundant extra replicas goes to the expert with the largest load per replica;
+    2. every replica carries load / replicas; replicas are taken heaviest first;
+    3. each goes to the least-loaded card that still has a free slot ((E + R) / n_cards per card).
+    Returns (replicas [E], slot_expert [E + R] card-major, slot_replica, card_load [n_cards])."""
+    load = [int(v) for v in load]
+    E = len(load)
+    reps = [1] * E
+    for _ in range(n_redundant):
+        best = 0
+        for e in range(1, E):
+            if load[e] / reps[e] > load[best] / reps[best]:
+                best = e
+        reps[best] += 1
+    copies = [(load[e] / reps[e], e) for e in range(E) for _ in range(reps[e])]
+    order = sorted(range(len(copies)), key=lambda i: (-copies[i][0], i))  # heaviest first, stable
+    per_card = (E + n_redundant) // n_cards
+    used = [0] * n_cards
+    card = [0.0] * n_cards
+    slot_expert = [-1] * (E + n_redundant)
+    slot_replica = [-1] * (E + n_redundant)
+    placed = [0] * E
+    for i in order:
+        w, e = copies[i]
+        g = min((c for c in range(n_cards) if used[c] < per_card), key=lambda c: (card[c], c))
+        slot = g * per_card + used[g]
+        slot_expert[slot], slot_replica[slot] = e, placed[e]
+        placed[e] += 1
+        used[g] += 1
+        card[g] += w
+    return (np.array(reps, np.int32), np.array(slot_expert, np.int32), np.array(slot_replica, np.int32),
+            np.array(card, np.float64))
+
+
+def permute_placed(topk_idx, E, slot_expert, slot_replica, replicas, cap=0):
+    """The permutation over physical slots: the r-th kept token (token order) of expert e goes to its
+    replica r % replicas[e], row r // replicas[e] of that slot; slots in slot order.
+    Returns (counts [S], offsets [S + 1], inv_pos [T, k], row_token [offsets[S]])."""
+    idx = np.asarray(topk_idx)
+    T, k = idx.shape
+    S = len(slot_expert)
+    slot_of = {(int(slot_expert[s]), int(slot_replica[s])): s for s in range(S)}
+    members = [[] for _ in range(S)]  # (token, slot j) per physical slot, in order
+    for e in range(E):
+        r = 0
+        for t in range(T):
+            for j in range(k):
+                if idx[t, j] == e:
+                    if cap <= 0 or r < cap:
+                        members[slot_of[(e, r % int(replicas[e]))]].append((t, j))
+                    r += 1
+    counts = np.array([len(m) for m in members], np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    inv_pos = np.full((T, k), -1, np.int32)
+    row_token = np.empty(int(offsets[-1]), np.int32)
+    for s in range(S):
+        for i, (t, j) in enumerate(members[s]):
+            inv_pos[t, j] = offsets[s] + i
+            row_token[offsets[s] + i] = t
+    return counts, offsets, inv_pos, row_token
+
+
 # ---------------------------------------------------------------- host-side statistics
+def placement_imbalance(card_load) -> float:
+    """Busiest card / mean card of a placement."""
+    c = np.asarray(card_load, np.float64)
+    return float(c.max() / c.mean())
+
+
 def imbalance(counts, n_cards) -> float:
     """Load imbalance of a contiguous expert placement: busiest card / mean card (1 = balanced).
     (Inference guide 6.4, section 5.1: the layer waits for the busiest card.)"""

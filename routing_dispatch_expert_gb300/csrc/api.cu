@@ -52,6 +52,13 @@ int check_config(const moe_config* c) {
   if (c->I_shared != 0 && c->I_shared != c->I) return fail(MOE_ERR_UNSUPPORTED, "I_shared must be 0 or I");
   if ((int64_t)c->T * (c->k + 1) > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "T * (k + 1) exceeds int32 rows");
   if (!(c->capacity_factor >= 0.f)) return fail(MOE_ERR_INVALID, "capacity_factor must be >= 0");
+  if (c->placement) {
+    const moe_placement* p = c->placement;
+    if (p->n_slots < c->E || p->n_slots > 1024 || p->max_replicas < 1)
+      return fail(MOE_ERR_INVALID, "placement: need E <= n_slots <= 1024 and max_replicas >= 1");
+    if (!p->slot_expert || !p->slot_replica || !p->replicas || !p->replica_slot)
+      return fail(MOE_ERR_INVALID, "placement: NULL table");
+  }
   return MOE_OK;
 }
 
@@ -60,9 +67,12 @@ struct Layout {
   int64_t R, R_tot;
 };
 
+// expert-major buffers are grouped per physical slot (one per expert without a placement)
+int64_t n_groups(const moe_config* c) { return c->placement ? c->placement->n_slots : c->E; }
+
 Layout make_layout(const moe_config* c) {
   Layout L;
-  const int64_t T = c->T, E = c->E, k = c->k, h = c->h, I = c->I;
+  const int64_t T = c->T, E = c->E, k = c->k, h = c->h, I = c->I, S = n_groups(c);
   const bool fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
   L.R = T * k;
   L.R_tot = L.R + (c->I_shared > 0 ? T : 0);
@@ -76,8 +86,8 @@ Layout make_layout(const moe_config* c) {
   l.logits = take(sizeof(float) * T * E);
   l.topk_idx = take(sizeof(int32_t) * T * k);
   l.topk_w = take(sizeof(float) * T * k);
-  l.counts = take(sizeof(int32_t) * E);
-  l.offsets = take(sizeof(int32_t) * (E + 1));
+  l.counts = take(sizeof(int32_t) * S);
+  l.offsets = take(sizeof(int32_t) * (S + 1));
   l.inv_pos = take(sizeof(int32_t) * T * k);
   l.row_token = take(sizeof(int32_t) * L.R);
   l.row_weight = take(sizeof(float) * L.R);
@@ -87,7 +97,7 @@ Layout make_layout(const moe_config* c) {
   l.h_scales = take(fp8 ? sizeof(float) * L.R_tot * (I / 128) : 0);
   l.yd = take(2 * L.R_tot * h);
   l.router_w3 = take(2 * 3 * E * h);
-  l.scratch = take(256 + sizeof(int32_t) * moe::dispatch_scratch_ints(c->T, c->E));
+  l.scratch = take(256 + sizeof(int32_t) * (moe::dispatch_scratch_ints(c->T, c->E) + E));
   l.total = o;
   return L;
 }
@@ -97,6 +107,22 @@ int* status_ptr(void* ws, const moe_ws_layout& l) {
 }
 int32_t* hist_ptr(void* ws, const moe_ws_layout& l) {
   return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + l.scratch + 256);
+}
+// kept rows per logical expert (placement only), after the histograms
+int32_t* expert_counts_ptr(void* ws, const moe_ws_layout& l, const moe_config* c) {
+  return hist_ptr(ws, l) + moe::dispatch_scratch_ints(c->T, c->E);
+}
+
+void set_placement(moe::DispatchDesc& d, const moe_config* c, int32_t* expert_counts) {
+  if (!c->placement) return;
+  const moe_placement* p = c->placement;
+  d.n_slots = p->n_slots;
+  d.max_replicas = p->max_replicas;
+  d.slot_expert = p->slot_expert;
+  d.slot_replica = p->slot_replica;
+  d.replicas = p->replicas;
+  d.replica_slot = p->replica_slot;
+  d.expert_counts = expert_counts;
 }
 
 template <class T>
@@ -208,6 +234,7 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   d.shared = c->I_shared > 0;
   d.fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
   d.capacity = capacity_of(c);
+  set_placement(d, c, expert_counts_ptr(ws, L.l, c));
   cudaError_t e = moe::launch_dispatch(d, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   if (c->T > 0) counted(4);
@@ -220,8 +247,12 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
   if (c->T == 0) return MOE_OK;
   const bool shared = c->I_shared > 0;
   std::string err;
+  const int S = (int)n_groups(c);
+  const int32_t* slot_expert = c->placement ? c->placement->slot_expert : nullptr;
   if (c->dtype == MOE_DTYPE_FP8_BLOCK128) {
     moe::GroupedGemmFp8Desc g;
+    g.slot_expert = slot_expert;
+    g.n_experts = c->E;
     g.A = xd;
     g.a_scales = xd_scales;
     g.a_rows = L.R_tot;
@@ -231,7 +262,7 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
     g.bs_scales = shared ? w->s_gu_shared : nullptr;
     g.b_rows = 2 * (int64_t)c->I;
     g.offsets = offsets;
-    g.E = c->E;
+    g.E = S;
     g.R = (int)L.R;
     g.T = c->T;
     g.K = c->h;
@@ -265,13 +296,15 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
     return MOE_OK;
   }
   moe::GroupedGemmDesc g;
+  g.slot_expert = slot_expert;
+  g.n_experts = c->E;
   g.A = xd;
   g.a_rows = L.R_tot;
   g.B = w->w_gu;
   g.Bs = shared ? w->w_gu_shared : nullptr;
   g.b_rows = 2 * (int64_t)c->I;
   g.offsets = offsets;
-  g.E = c->E;
+  g.E = S;
   g.R = (int)L.R;
   g.T = c->T;
   g.K = c->h;
@@ -522,6 +555,15 @@ MOE_EXPORT int moe_quantize_weights_fp8(const void* w, int64_t batch, int64_t ro
   return MOE_OK;
 }
 
+MOE_EXPORT int moe_eplb_plan(const int64_t* load, int32_t E, int32_t n_cards, int32_t n_redundant, int32_t* replicas,
+                             int32_t* slot_expert, int32_t* slot_replica, int32_t* replica_slot, double* card_load) {
+  std::string err;
+  const int rc = moe::eplb_plan(load, E, n_cards, n_redundant, replicas, slot_expert, slot_replica, replica_slot,
+                                card_load, &err);
+  if (rc) return fail(rc, err);
+  return MOE_OK;
+}
+
 MOE_EXPORT int moe_device_status(const moe_config* cfg, void* ws, int32_t* status, moe_stream_t stream) {
   int rc = check_config(cfg);
   if (rc) return rc;
@@ -587,9 +629,9 @@ MOE_EXPORT int moe_dispatch_noalloc(const moe_config* cfg, const void* x, const 
                                     moe_stream_t stream) {
   int rc = check_config(cfg);
   if (rc) return rc;
-  const size_t need = moe::dispatch_scratch_ints(cfg->T, cfg->E);
+  const size_t need = moe::dispatch_scratch_ints(cfg->T, cfg->E) + cfg->E;
   if (need > kNoAllocHistInts)
-    return fail(MOE_ERR_UNSUPPORTED, "moe_dispatch_noalloc: ceil(T / 512) * E = " + std::to_string(need) +
+    return fail(MOE_ERR_UNSUPPORTED, "moe_dispatch_noalloc: (ceil(T / 512) + 1) * E = " + std::to_string(need) +
                                          " histogram entries exceed the static scratch of " +
                                          std::to_string(kNoAllocHistInts) + "; use moe_dispatch with a workspace");
   REQUIRE_PTR(x, "x");
@@ -629,6 +671,7 @@ MOE_EXPORT int moe_dispatch_noalloc(const moe_config* cfg, const void* x, const 
   d.shared = cfg->I_shared > 0;
   d.fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
   d.capacity = capacity_of(cfg);
+  set_placement(d, cfg, d.scratch + moe::dispatch_scratch_ints(cfg->T, cfg->E));
   e = moe::launch_dispatch(d, s);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   if (cfg->T > 0) counted(4);

@@ -48,11 +48,18 @@ __global__ void __launch_bounds__(TPB) hist_kernel(const int32_t* __restrict__ i
 }
 
 // hist[b][e] becomes the number of earlier tokens (blocks < b) that chose e, i.e. the rank within
-// expert e of block b's first such token; counts are clamped to the capacity `cap`.
+// expert e of block b's first such token; counts are clamped to the capacity `cap`. With a placement
+// the counts and offsets are per physical slot: replica i of an expert with R replicas and c kept rows
+// gets the rows of ranks i, i + R, i + 2R, ... < c.
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nblk, int E, int cap,
-                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                    int n_slots, const int32_t* __restrict__ slot_expert,
+                                                    const int32_t* __restrict__ slot_replica,
+                                                    const int32_t* __restrict__ replicas,
+                                                    int32_t* __restrict__ expert_counts) {
   __shared__ int32_t warp_tot[32];
-  const int e = threadIdx.x;  // E <= 1024
+  __shared__ int32_t kept[1024];
+  const int e = threadIdx.x;  // E <= 1024, n_slots <= 1024
   int run = 0;
   if (e < E) {
     for (int b = 0; b < nblk; ++b) {
@@ -61,7 +68,20 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
       run += c;
     }
     run = min(run, cap);
-    counts[e] = run;
+    if (n_slots == 0)
+      counts[e] = run;
+    else
+      expert_counts[e] = kept[e] = run;
+  }
+  const int n = n_slots == 0 ? E : n_slots;
+  if (n_slots != 0) {
+    __syncthreads();
+    run = 0;
+    if (e < n_slots) {
+      const int ex = slot_expert[e], i = slot_replica[e], r = replicas[ex], c = kept[ex];
+      run = c > i ? (c - i + r - 1) / r : 0;
+      counts[e] = run;
+    }
   }
   // exclusive scan of run over experts
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -85,14 +105,16 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
   }
   __syncthreads();
   const int excl = warp_tot[w] + incl - run;
-  if (e < E) offsets[e] = excl;
-  if (e == E - 1) offsets[E] = excl + run;
+  if (e < n) offsets[e] = excl;
+  if (e == n - 1) offsets[n] = excl + run;
 }
 
 __global__ void __launch_bounds__(TPB) rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
                                                    const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
                                                    int T, int k, int E, int cap, int32_t* __restrict__ inv_pos,
-                                                   int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
+                                                   int32_t* __restrict__ row_token, float* __restrict__ row_weight,
+                                                   int n_slots, int max_replicas, const int32_t* __restrict__ replicas,
+                                                   const int32_t* __restrict__ replica_slot) {
   extern __shared__ uint32_t smem[];
   uint32_t* masks = smem;                                        // [WARPS][E]
   int32_t* wbase = reinterpret_cast<int32_t*>(smem + WARPS * E);  // [WARPS][E]
@@ -123,7 +145,12 @@ __global__ void __launch_bounds__(TPB) rank_kernel(const int32_t* __restrict__ i
       if (e >= 0 && e < E) {
         const int rank = wbase[w * E + e] + __popc(masks[w * E + e] & lt);  // earlier tokens choosing e
         if (rank < cap) {
-          row = offsets[e] + rank;
+          if (n_slots == 0) {
+            row = offsets[e] + rank;
+          } else {  // round-robin over the expert's replicas
+            const int r = replicas[e];
+            row = offsets[replica_slot[e * max_replicas + rank % r]] + rank / r;
+          }
           row_token[row] = (int32_t)t;
           row_weight[row] = topk_w[t * k + j];
         }
@@ -221,14 +248,16 @@ size_t dispatch_scratch_ints(int T, int E) { return (size_t)dispatch_blocks(T) *
 cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
   if (d.T == 0) {
     // no tokens: offsets must still describe E empty experts
-    cudaError_t e = cudaMemsetAsync(d.counts, 0, sizeof(int32_t) * d.E, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(d.offsets, 0, sizeof(int32_t) * (d.E + 1), stream);
+    const int n = d.n_slots ? d.n_slots : d.E;
+    cudaError_t e = cudaMemsetAsync(d.counts, 0, sizeof(int32_t) * n, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d.offsets, 0, sizeof(int32_t) * (n + 1), stream);
     return e;
   }
   const int nblk = dispatch_blocks(d.T);
   dp::hist_kernel<<<nblk, dp::TPB, sizeof(int32_t) * d.E, stream>>>(d.topk_idx, d.T, d.k, d.E, d.scratch, d.status);
   const int cap = d.capacity > 0 ? d.capacity : 0x7fffffff;
-  dp::scan_kernel<<<1, 1024, 0, stream>>>(d.scratch, nblk, d.E, cap, d.counts, d.offsets);
+  dp::scan_kernel<<<1, 1024, 0, stream>>>(d.scratch, nblk, d.E, cap, d.counts, d.offsets, d.n_slots, d.slot_expert,
+                                          d.slot_replica, d.replicas, d.expert_counts);
   const size_t rank_smem = sizeof(uint32_t) * 2 * dp::WARPS * d.E;
   static bool attr = false;
   if (!attr) {
@@ -238,7 +267,8 @@ cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
     attr = true;
   }
   dp::rank_kernel<<<nblk, dp::TPB, rank_smem, stream>>>(d.topk_idx, d.topk_w, d.scratch, d.offsets, d.T, d.k, d.E,
-                                                         cap, d.inv_pos, d.row_token, d.row_weight);
+                                                         cap, d.inv_pos, d.row_token, d.row_weight, d.n_slots,
+                                                         d.max_replicas, d.replicas, d.replica_slot);
   int64_t blocks = cdiv(d.T, 8);
   if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
   const int R = d.T * d.k;

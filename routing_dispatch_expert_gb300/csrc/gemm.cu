@@ -63,6 +63,7 @@ struct Args {
   int T;
   int K;        // reduction length (multiple of BK)
   int n_tiles;  // output column tiles per group
+  const int32_t* slot_expert;  // routed group -> logical expert whose weights it uses (nullptr: identity)
   int mode;     // 0: gate/up + SwiGLU -> H; 1: down * row_weight -> yd; 2: router, fp32 out
   int I;        // mode 0: row offset of the up half inside W_gu
   int ksplit;   // B is split into ksplit K passes over the same A (mode 2: 3), else 1
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM, args.mode == 2);
       const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
-      const int zg = t.g < args.E ? t.g : 0;
+      const int zg = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) : 0;
       int n0, n1;
       if (args.mode == 0) {
         n0 = t.n_tile * (BN / 2);
@@ -430,7 +431,8 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int ksplit = d.ksplit > 1 ? d.ksplit : 1;
   bool ok = tma_encode_2d(&tA, d.A, BF, 2, d.a_rows, d.K, gg::BM) &&
-            tma_encode_3d(&tB, d.B, BF, 2, ksplit > 1 ? ksplit : d.E, d.b_rows, d.K, gg::BN / 2) &&
+            tma_encode_3d(&tB, d.B, BF, 2, ksplit > 1 ? ksplit : (d.n_experts > 0 ? d.n_experts : d.E), d.b_rows,
+                          d.K, gg::BN / 2) &&
             tma_encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, gg::BN / 2);
   if (!ok) {
     *err = "cuTensorMapEncodeTiled rejected a grouped-GEMM operand";
@@ -444,6 +446,7 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.T = d.T;
   a.K = d.K;
   a.mode = d.mode;
+  a.slot_expert = d.slot_expert;
   a.I = d.I;
   a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, d.mode == 2 ? gg::BN / 2 : gg::BN);
   a.ksplit = ksplit;

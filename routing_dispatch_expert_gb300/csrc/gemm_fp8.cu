@@ -45,6 +45,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 
 struct Args {
   const int32_t* offsets;
+  const int32_t* slot_expert;  // routed group -> logical expert (nullptr: identity)
   int E, shared, R, T, K, n_tiles, mode, I, ldo;
   void* out;               // mode 0: H codes [R_tot, I]; mode 1: yd bf16 [R_tot, ldo]
   float* out_scales;       // mode 0: H scales [R_tot, I / 128]
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
       const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
-      const int z = t.g < args.E ? t.g : 0;
+      const int z = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) : 0;
       int n0, n1;
       if (args.mode == 0) {
         n0 = t.n_tile * (BN / 2);
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t row = (int64_t)t.a_row + r;
       // scale indices (32-bit: R_tot * K/128 and E * nb * K/128 stay far below 2^31)
       const float* bsc = t.g < args.E ? args.b_scales : args.bs_scales;
-      const int gbase = t.g < args.E ? t.g * args.nb * KB : 0;
+      const int gbase = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) * args.nb * KB : 0;
       const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + (part >> 1);
       const int nb_hi = args.mode == 0 ? args.I / 128 + t.n_tile : nb_lo;
       const int ia = (int)row * KB;
@@ -347,7 +348,7 @@ cudaError_t launch_grouped_gemm_fp8(const GroupedGemmFp8Desc& d, cudaStream_t st
   CUtensorMap tA, tB, tBs;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   bool ok = tma_encode_2d(&tA, d.A, U8, 1, d.a_rows, d.K, g8::BM) &&
-            tma_encode_3d(&tB, d.B, U8, 1, d.E, d.b_rows, d.K, g8::BN / 2) &&
+            tma_encode_3d(&tB, d.B, U8, 1, d.n_experts > 0 ? d.n_experts : d.E, d.b_rows, d.K, g8::BN / 2) &&
             tma_encode_3d(&tBs, d.Bs ? d.Bs : d.B, U8, 1, 1, d.b_rows, d.K, g8::BN / 2);
   if (!ok) {
     *err = "cuTensorMapEncodeTiled rejected an FP8 grouped-GEMM operand";
@@ -355,6 +356,7 @@ cudaError_t launch_grouped_gemm_fp8(const GroupedGemmFp8Desc& d, cudaStream_t st
   }
   g8::Args a;
   a.offsets = d.offsets;
+  a.slot_expert = d.slot_expert;
   a.E = d.E;
   a.shared = d.Bs != nullptr;
   a.R = d.R;

@@ -10,6 +10,10 @@ namespace moe {
 
 int num_sms();
 
+// EPLB placement plan on the host (eplb.cu).
+int eplb_plan(const int64_t* load, int E, int n_cards, int n_redundant, int32_t* replicas, int32_t* slot_expert,
+              int32_t* slot_replica, int32_t* replica_slot, double* card_load, std::string* err);
+
 // Step 1: router GEMM, logits[T, E] = x[T, h] (bf16) . w_r[E, h]^T (fp32), fp32 accumulation.
 cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, int T, int h, int E,
                                cudaStream_t stream);
@@ -49,6 +53,14 @@ struct DispatchDesc {
   int shared;  // also write the T token rows for the shared expert
   int fp8;
   int capacity = 0;  // > 0: keep at most this many rows per expert (earliest tokens)
+  // placement (all null: one slot per expert)
+  int n_slots = 0;
+  int max_replicas = 0;
+  const int32_t* slot_expert = nullptr;
+  const int32_t* slot_replica = nullptr;
+  const int32_t* replicas = nullptr;
+  const int32_t* replica_slot = nullptr;
+  int32_t* expert_counts = nullptr;  // scratch [E]: kept rows per logical expert
 };
 cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream);
 
@@ -60,6 +72,8 @@ struct GroupedGemmDesc {
   const void* Bs;  // [b_rows, K] shared expert or nullptr
   int64_t b_rows;
   const int32_t* offsets;  // nullptr: a single group of rows [0, T) (router)
+  const int32_t* slot_expert = nullptr;  // group -> logical expert (weights), nullptr: identity
+  int n_experts = 0;                     // logical experts in B (0: E)
   int E, R, T, K, N, I;
   int mode;  // 0 gate/up -> H, 1 down -> yd, 2 router logits (fp32)
   int ksplit = 1;  // mode 2: B holds 3 bf16 terms of the fp32 weight, [3, N, K]
@@ -82,6 +96,8 @@ struct GroupedGemmFp8Desc {
   const float* bs_scales;
   int64_t b_rows;
   const int32_t* offsets;
+  const int32_t* slot_expert = nullptr;
+  int n_experts = 0;
   int E, R, T, K, N, I;
   int mode;
   void* out;

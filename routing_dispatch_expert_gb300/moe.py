@@ -28,11 +28,17 @@ class MoeError(RuntimeError):
         self.code = code
 
 
+class MoePlacement(ctypes.Structure):
+    _fields_ = [("n_slots", ctypes.c_int32), ("max_replicas", ctypes.c_int32), ("slot_expert", ctypes.c_void_p),
+                ("slot_replica", ctypes.c_void_p), ("replicas", ctypes.c_void_p), ("replica_slot", ctypes.c_void_p)]
+
+
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("h", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("score", ctypes.c_int32), ("renormalize", ctypes.c_int32),
-                ("routed_scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("capacity_factor", ctypes.c_float)]
+                ("routed_scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+                ("placement", ctypes.POINTER(MoePlacement))]
 
 
 class MoeWeightsStruct(ctypes.Structure):
@@ -75,6 +81,7 @@ def load():
                 "moe_graph_create": [cfgp, vp, wp, vp, vp, sz, vp, ctypes.POINTER(vp)],
                 "moe_graph_launch": [vp, vp],
                 "moe_graph_destroy": [vp],
+                "moe_eplb_plan": [vp, i32, i32, i32, vp, vp, vp, vp, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -102,11 +109,45 @@ def _stream():
 
 
 def make_config(T, h, E, k, I, I_shared=0, n_group=1, topk_group=1, score="softmax", renorm=False, routed_scale=1.0,
-                dtype="bf16", capacity_factor=0.0) -> MoeConfig:
-    return MoeConfig(T, h, E, k, I, I_shared, n_group, topk_group,
-                     MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID, int(bool(renorm)),
-                     float(routed_scale), MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP8_BLOCK128,
-                     float(capacity_factor))
+                dtype="bf16", capacity_factor=0.0, placement: "Placement | None" = None) -> MoeConfig:
+    cfg = MoeConfig(T, h, E, k, I, I_shared, n_group, topk_group,
+                    MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID, int(bool(renorm)),
+                    float(routed_scale), MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP8_BLOCK128,
+                    float(capacity_factor), None if placement is None else ctypes.pointer(placement.struct))
+    cfg._placement = placement  # keep the tables alive as long as the config
+    return cfg
+
+
+def eplb_plan(load, n_cards: int, n_redundant: int) -> dict:
+    """moe_eplb_plan on the host: numpy arrays replicas [E], slot_expert / slot_replica [E + R],
+    replica_slot [E, R + 1], card_load [n_cards]."""
+    import numpy as np
+
+    load = np.ascontiguousarray(load, dtype=np.int64)
+    E = load.size
+    S = E + n_redundant
+    out = dict(replicas=np.empty(E, np.int32), slot_expert=np.empty(S, np.int32), slot_replica=np.empty(S, np.int32),
+               replica_slot=np.empty((E, n_redundant + 1), np.int32), card_load=np.empty(n_cards, np.float64))
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
+    _check(load_lib_eplb()(p(load), E, n_cards, n_redundant, p(out["replicas"]), p(out["slot_expert"]),
+                           p(out["slot_replica"]), p(out["replica_slot"]), p(out["card_load"])))
+    return out
+
+
+def load_lib_eplb():
+    return load().moe_eplb_plan
+
+
+class Placement:
+    """Device copy of an EPLB plan (see eplb_plan) and its C struct, for make_config(placement=...)."""
+
+    def __init__(self, plan: dict, device="cuda"):
+        self.tables = {k: torch.from_numpy(plan[k]).to(device) for k in ("slot_expert", "slot_replica", "replicas",
+                                                                          "replica_slot")}
+        self.n_slots = int(plan["slot_expert"].size)
+        self.struct = MoePlacement(self.n_slots, int(plan["replica_slot"].shape[1]),
+                                   self.tables["slot_expert"].data_ptr(), self.tables["slot_replica"].data_ptr(),
+                                   self.tables["replicas"].data_ptr(), self.tables["replica_slot"].data_ptr())
 
 
 class Weights:

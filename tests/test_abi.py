@@ -39,7 +39,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_sizes_match_header_layout():
-    assert ctypes.sizeof(moe.MoeConfig) == 13 * 4
+    assert ctypes.sizeof(moe.MoeConfig) == 13 * 4 + 4 + 8  # 13 scalars, padding, placement pointer
+    assert ctypes.sizeof(moe.MoePlacement) == 2 * 4 + 4 * 8
     assert ctypes.sizeof(moe.MoeWeightsStruct) == 10 * 8
     assert ctypes.sizeof(moe.MoeWsLayout) == 16 * 8
 
@@ -96,3 +97,27 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     rc = lib.moe_quantize_weights_fp8(ctypes.c_void_p(0x1000), 1, 100, 128, ctypes.c_void_p(0x1000),
                                       ctypes.c_void_p(0x1000), None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_eplb_plan_host_entry_point_matches_oracle(lib):
+    """moe_eplb_plan runs on the host: checked here without a GPU against the oracle's planner."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(5)
+    for E, cards, red in ((256, 8, 0), (256, 32, 32), (64, 8, 8), (16, 4, 4), (12, 3, 0)):
+        load = rng.integers(0, 500, E)
+        load[rng.integers(0, E)] = 3000  # one hot expert
+        got = moe.eplb_plan(load, cards, red)
+        reps, slot_expert, slot_replica, card = oracle.eplb_plan(load, cards, red)
+        np.testing.assert_array_equal(got["replicas"], reps)
+        np.testing.assert_array_equal(got["slot_expert"], slot_expert)
+        np.testing.assert_array_equal(got["slot_replica"], slot_replica)
+        np.testing.assert_array_equal(got["card_load"], card)
+        for e in range(E):  # replica_slot is the inverse of (slot_expert, slot_replica)
+            for i in range(reps[e]):
+                s = got["replica_slot"][e, i]
+                assert slot_expert[s] == e and slot_replica[s] == i
+    rc = lib.moe_eplb_plan(None, 8, 3, 0, None, None, None, None, None)
+    assert rc == moe.MOE_ERR_INVALID

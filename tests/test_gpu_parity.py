@@ -328,3 +328,41 @@ def test_routing_near_ties_bit_exact(score):
     ri, rw = oracle.route(logits, bias, **route_kwargs(wl))
     np.testing.assert_array_equal(idx.cpu().numpy(), ri)
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("dtype,cf", [("bf16", 0.0), ("fp8", 0.0), ("bf16", 1.1)])
+def test_eplb_placement_matches_unplaced_layer(dtype, cf):
+    """An EPLB placement (redundant replicas, card-major slots) only reorders the expert-major rows:
+    the per-slot permutation matches the oracle and the layer output is bit-identical."""
+    base = synth.WORKLOADS["dsv3_decode"].replace(T=400, h=512, E=64, I=256, I_shared=256, zipf_s=1.2,
+                                                  dtype=dtype, capacity_factor=cf)
+    L = GpuLayer(base)
+    y0 = L.forward().clone()
+    it0 = L.intermediates()
+    idx = it0["topk_idx"].cpu().numpy()
+    load = np.bincount(idx.ravel(), minlength=base.E)
+    plan = rde.eplb_plan(load, n_cards=8, n_redundant=8)
+    pl = rde.Placement(plan)
+    cfg = rde.make_config(T=base.T, h=base.h, E=base.E, k=base.k, I=base.I, I_shared=base.I_shared,
+                          n_group=base.n_group, topk_group=base.topk_group, score=base.score, renorm=base.renorm,
+                          routed_scale=base.routed_scale, dtype=dtype, capacity_factor=cf, placement=pl)
+    ws = rde.alloc_workspace(cfg)
+    rde.device_status(cfg, ws)
+    y = torch.empty_like(y0)
+    rde.forward(cfg, L.inp["x"], L.weights, y, ws)
+    torch.cuda.synchronize()
+    assert rde.device_status(cfg, ws) == 0
+    S = pl.n_slots
+    counts = rde.ws_view(ws, cfg, "counts", torch.int32, (S,)).cpu().numpy()
+    offsets = rde.ws_view(ws, cfg, "offsets", torch.int32, (S + 1,)).cpu().numpy()
+    inv_pos = rde.ws_view(ws, cfg, "inv_pos", torch.int32, (base.T, base.k)).cpu().numpy()
+    cap = oracle.capacity(cf, base.T, base.k, base.E)
+    rc, ro, ri, rt = oracle.permute_placed(idx, base.E, plan["slot_expert"], plan["slot_replica"], plan["replicas"],
+                                           cap)
+    np.testing.assert_array_equal(counts, rc)
+    np.testing.assert_array_equal(offsets, ro)
+    np.testing.assert_array_equal(inv_pos, ri)
+    row_token = rde.ws_view(ws, cfg, "row_token", torch.int32, (base.T * base.k,)).cpu().numpy()
+    np.testing.assert_array_equal(row_token[:ro[-1]], rt)
+    assert plan["replicas"].max() > 1  # the hot experts really got replicas
+    assert torch.equal(y.view(torch.int16), y0.view(torch.int16))

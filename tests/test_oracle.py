@@ -406,3 +406,40 @@ def test_capacity_above_the_largest_load_is_dropless():
     b = oracle.permute_capacity(idx, 16, 10 ** 6)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u, v)
+
+
+# ------------------------------------------------------------------------------------ placement
+def test_p5_placement_table():
+    """The page's table: busiest card / mean after rebalancing, and with one redundant expert per
+    card, reproduced by the oracle's planner on the seeded loads."""
+    g = json.load(open(os.path.join(GOLDEN, "p5_imbalance.json")))
+    c = _p5_sampler(g["experts"], g["top_k"], g["tokens"], g["skew"], g["seed"])
+    for ep, val in g["rebalance_imbalance"].items():
+        _, _, _, card = oracle.eplb_plan(c, int(ep), 0)
+        assert round(oracle.placement_imbalance(card), 2) == pytest.approx(val), ep
+    for ep, val in g["redundant_imbalance"].items():
+        reps, slot_expert, _, card = oracle.eplb_plan(c, int(ep), int(ep))
+        assert reps.sum() == g["experts"] + int(ep)
+        assert round(oracle.placement_imbalance(card), 2) == pytest.approx(val), ep
+
+
+def test_placed_permutation_round_robin():
+    rng = np.random.default_rng(17)
+    T, E, k = 120, 8, 2
+    idx = np.stack([rng.choice(E, k, replace=False, p=[.5, .2, .1, .05, .05, .04, .03, .03])
+                    for _ in range(T)]).astype(np.int32)
+    load = np.bincount(idx.ravel(), minlength=E)
+    reps, slot_expert, slot_replica, _ = oracle.eplb_plan(load, 2, 2)
+    counts, offsets, inv_pos, row_token = oracle.permute_placed(idx, E, slot_expert, slot_replica, reps)
+    assert counts.sum() == T * k and sorted(inv_pos.ravel()) == list(range(T * k))
+    np.testing.assert_array_equal(row_token[inv_pos], np.repeat(np.arange(T), k).reshape(T, k))
+    for s in range(len(slot_expert)):  # slot s holds every reps-th token of its expert, in order
+        e, i = slot_expert[s], slot_replica[s]
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        np.testing.assert_array_equal(row_token[offsets[s]:offsets[s + 1]], toks[i::reps[e]])
+    # without redundancy and in expert order, the placed permutation is the plain one
+    ident = np.arange(E, dtype=np.int32)
+    a = oracle.permute_placed(idx, E, ident, np.zeros(E, np.int32), np.ones(E, np.int32))
+    b = oracle.permute(idx, E)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
