@@ -12,12 +12,16 @@ namespace grp {
 
 constexpr int MAX_GROUPS = 1025;  // E <= 1024 routed experts + the shared expert
 
-// gtile[g]: exclusive prefix of 128-row tiles over groups; grow[g]: first row of group g (grow[G] =
-// end row). Groups: the E routed experts (rows [offsets[e], offsets[e+1])) and, with a shared expert,
-// group E = rows [R, R + T). offsets == nullptr means one group of rows [0, T).
+// gtile[g]: exclusive prefix of 128-row tiles over groups; grow[g]: first row of group g; gend:
+// one past the last row of the last routed group (offsets[E]; with a capacity limit it can lie below
+// R, the shared expert's first row). Groups: the E routed experts (rows [offsets[e], offsets[e+1]))
+// and, with a shared expert, group E = rows [R, R + T). offsets == nullptr means one group of rows
+// [0, T).
 struct Table {
   int gtile[MAX_GROUPS + 1];
   int grow[MAX_GROUPS + 1];
+  int n_routed;  // groups whose rows come from offsets (E, or 0 when offsets == nullptr)
+  int gend;
 };
 
 struct Tile {
@@ -60,6 +64,8 @@ __device__ __forceinline__ void build_table(Table& tb, const int32_t* offsets, i
   if (lane == 0) {
     tb.gtile[G] = carry;
     tb.grow[G] = offsets == nullptr ? T : (shared ? R + T : offsets[E]);
+    tb.n_routed = offsets == nullptr ? 0 : E;
+    tb.gend = offsets == nullptr ? T : offsets[E];
   }
 }
 
@@ -88,8 +94,8 @@ __device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int 
     t.m_tile = local - t.n_tile * mtc;
   }
   t.a_row = tb.grow[lo] + t.m_tile * BM;
-  const int m = tb.grow[lo + 1] - tb.grow[lo];
-  t.rows = min(BM, m - t.m_tile * BM);
+  const int end = lo + 1 == tb.n_routed ? tb.gend : tb.grow[lo + 1];
+  t.rows = min(BM, end - t.a_row);
   return t;
 }
 

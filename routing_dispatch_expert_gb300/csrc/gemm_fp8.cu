@@ -13,8 +13,11 @@
 // product in a fresh TMEM partial (2 x 256 columns, double buffered) and sixteen epilogue warps
 // promote it: acc += partial * sa[row, kb] * sb[n_block, kb], in fp32 registers (64 per thread; four
 // warps share each TMEM lane quarter, one per quarter of the columns; two accumulators per packed
-// fma.rn.f32x2). The MMA of block kb+1 overlaps the promotion of block kb; four promotion warps per
-// SM sub-partition hide the TMEM-load latency.
+// IEEE fma of a float2). The MMA of block kb+1 overlaps the promotion of block kb; four promotion
+// warps per SM sub-partition hide the TMEM-load latency. The partial is read 8 columns at a time so
+// that 64 accumulators plus the loaded values fit the 96 registers a 576-thread CTA allows without
+// spilling (spilled values compete with the 192 KB TMA ring for the SM's L1), and the TMEM buffer is
+// handed back as soon as its last columns are in registers.
 //   * mode 0: each thread holds 32 gate and the 32 matching up columns of its row, so SwiGLU is local;
 //     the 128-column amax of H is shared by the four warps of a row through shared memory and a
 //     bounded mbarrier (never a blocking bar.sync, so a timed-out warp cannot hang the others).
@@ -72,15 +75,6 @@ struct Shared {
 };
 
 using grp::wait_or_abort;
-
-// acc0 += v0 * s, acc1 += v1 * s (two IEEE fma, one instruction)
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float v0, float v1, float s) {
-  asm("{\n\t.reg .b64 ra, rv, rs;\n\t"
-      "mov.b64 ra, {%0, %1};\n\tmov.b64 rv, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\t"
-      "fma.rn.f32x2 ra, rv, rs, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(v0), "f"(v1), "f"(s));
-}
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -201,30 +195,39 @@ __global__ void __launch_bounds__(THREADS, 1)
     // mode 0: gate columns [32 part, +32) and the matching up columns; mode 1: columns [64 part, +64)
     const int col_a = args.mode == 0 ? part * 32 : part * 64;
     const int col_b = args.mode == 0 ? BN / 2 + part * 32 : part * 64 + 32;
+    const uint32_t tq = tmem_base + ((uint32_t)(quarter * 32) << 16);  // this warp's TMEM lane quarter
+    const uint32_t tqa = tq + (uint32_t)col_a, tqb = tq + (uint32_t)col_b;
     const int KB = kblocks;
+    const int R_tot = args.R + (args.shared ? args.T : 0);
     int p = 0, tpar = 0;
     uint32_t pphase = 0, xphase = 0;
     bool fine = true;
     for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
-      const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
-      const bool valid = r < t.rows;
-      const int64_t row = (int64_t)t.a_row + r;
-      // scale indices (32-bit: R_tot * K/128 and E * nb * K/128 stay far below 2^31)
-      const float* bsc = t.g < args.E ? args.b_scales : args.bs_scales;
-      const int gbase = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) * args.nb * KB : 0;
-      const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + (part >> 1);
-      const int nb_hi = args.mode == 0 ? args.I / 128 + t.n_tile : nb_lo;
-      const int ia = (int)row * KB;
-      const int il = gbase + nb_lo * KB;
-      const int ih = gbase + nb_hi * KB;
+      // scale pointers of this tile (32-bit indices: R_tot * K/128 and E * nb * K/128 stay far below
+      // 2^31); rows past the buffer read the last row's scales and are never stored
+      const float* sar;
+      const float* sbl;
+      const float* sbh;
+      {
+        const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+        const float* bsc = t.g < args.E ? args.b_scales : args.bs_scales;
+        const int gbase = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) * args.nb * KB : 0;
+        const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + (part >> 1);
+        const int nb_hi = args.mode == 0 ? args.I / 128 + t.n_tile : nb_lo;
+        sar = args.a_scales + min(t.a_row + r, R_tot - 1) * KB;
+        sbl = bsc + gbase + nb_lo * KB;
+        sbh = bsc + gbase + nb_hi * KB;
+      }
 
-      float acc[64];
+      // acc[i] holds columns (2i, 2i+1) of this thread's 64: [0, 16) the col_a block, [16, 32) col_b
+      float2 acc[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-      float sa_n = valid ? args.a_scales[ia] : 0.f;  // the row scale is prefetched one K block ahead
+      for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+      float sa_n = sar[0];  // the row scale is prefetched one K block ahead
       for (int kb = 0; kb < KB; ++kb) {
-        const float s_lo = sa_n * bsc[il + kb], s_hi = sa_n * bsc[ih + kb];
-        if (kb + 1 < KB) sa_n = valid ? args.a_scales[ia + kb + 1] : 0.f;
+        const float s_lo = sa_n * sbl[kb], s_hi = sa_n * sbh[kb];
+        sa_n = sar[min(kb + 1, KB - 1)];
+        const float2 slo = make_float2(s_lo, s_lo), shi = make_float2(s_hi, s_hi);
         int ok = 1;
         if (lane == 0) ok = wait_or_abort(&s.pfull[p], pphase, &s.abort_flag, args.status, args.wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -234,33 +237,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(p * BN);
+        const uint32_t pofs = (uint32_t)(p * BN);
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(taddr + col_a + c, v);
-          tmem_ld_wait();
+        for (int g = 0; g < 8; ++g) {
+          uint32_t v[8];
+          tmem_ld8((g < 4 ? tqa : tqb) + pofs + (g & 3) * 8, v);
+          tmem_ld_wait_regs(v);
+          if (g == 7) {
+            // the partial is in registers: hand the TMEM buffer back before the last multiply-adds
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.pempty[p]);
+          }
 #pragma unroll
-          for (int i = 0; i < 16; i += 2)
-            ffma2(acc[c + i], acc[c + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s_lo);
+          for (int i = 0; i < 4; ++i)
+            acc[4 * g + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                        g < 4 ? slo : shi, acc[4 * g + i]);
         }
-#pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(taddr + col_b + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; i += 2)
-            ffma2(acc[32 + c + i], acc[32 + c + i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s_hi);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.pempty[p]);
         p ^= 1;
         if (p == 0) pphase ^= 1;
       }
       if (!fine) break;
 
+      const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      const bool valid = r < t.rows;
+      const int64_t row = (int64_t)t.a_row + r;
       if (args.mode == 1) {
         const float w = (valid && t.g < args.E) ? args.row_weight[row] : 1.0f;
         if (valid) {
@@ -268,18 +269,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                 t.n_tile * BN + part * 64);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * w, acc[8 * i + 1] * w),
-                                pack_bf16x2(acc[8 * i + 2] * w, acc[8 * i + 3] * w),
-                                pack_bf16x2(acc[8 * i + 4] * w, acc[8 * i + 5] * w),
-                                pack_bf16x2(acc[8 * i + 6] * w, acc[8 * i + 7] * w));
+            dst[i] = make_uint4(pack_bf16x2(acc[4 * i].x * w, acc[4 * i].y * w),
+                                pack_bf16x2(acc[4 * i + 1].x * w, acc[4 * i + 1].y * w),
+                                pack_bf16x2(acc[4 * i + 2].x * w, acc[4 * i + 2].y * w),
+                                pack_bf16x2(acc[4 * i + 3].x * w, acc[4 * i + 3].y * w));
         }
       } else {
         // SwiGLU on this thread's 32 columns, then the row's 128-column amax shared by the four parts
+        float h[32];
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          acc[i] = grp::silu(acc[i]) * acc[32 + i];
-          amax = fmaxf(amax, fabsf(acc[i]));
+        for (int i = 0; i < 16; ++i) {
+          h[2 * i] = grp::silu(acc[i].x) * acc[16 + i].x;
+          h[2 * i + 1] = grp::silu(acc[i].y) * acc[16 + i].y;
+          amax = fmaxf(amax, fmaxf(fabsf(h[2 * i]), fabsf(h[2 * i + 1])));
         }
         s.amax[tpar][part][r] = amax;
         __syncwarp();
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t w4 = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              w4 |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(acc[4 * i + j], scale), __NV_SATFINITE, __NV_E4M3)
+              w4 |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(h[4 * i + j], scale), __NV_SATFINITE, __NV_E4M3)
                     << (8 * j);
             q[i] = w4;
           }
