@@ -241,6 +241,15 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   return MOE_OK;
 }
 
+// bf16 expert GEMMs: CTA-pair tiles (256 rows) keep the tensor pipe busier than single-CTA tiles (128
+// rows) but pad each expert's last tile to 256 rows: they pay off once the experts average at least
+// this many rows. (The FP8 kernel stays on single CTAs: its per-K-block promotion hand-off would have
+// to cross the pair every 128 K elements.)
+constexpr int64_t kPairMinRowsPerGroup = 1024;
+bool use_pair_tiles(const moe_config* c, int S) {
+  return S > 0 && (int64_t)c->T * c->k >= kPairMinRowsPerGroup * S;
+}
+
 int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, const float* xd_scales,
                   const int32_t* offsets, const float* row_weight, void* yd, void* ws, const Layout& L,
                   cudaStream_t stream) {
@@ -295,6 +304,7 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
     counted(2);
     return MOE_OK;
   }
+  auto launch = use_pair_tiles(c, S) ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
   moe::GroupedGemmDesc g;
   g.slot_expert = slot_expert;
   g.n_experts = c->E;
@@ -315,7 +325,7 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
   g.ldo = c->I;
   g.row_weight = nullptr;
   g.status = status_ptr(ws, L.l);
-  cudaError_t e = moe::launch_grouped_gemm_bf16(g, stream, &err);
+  cudaError_t e = launch(g, stream, &err);
   if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "gate/up grouped GEMM launch") : cuda_fail(e, err.c_str());
   g.A = at<void>(ws, L.l.hbuf);
   g.B = w->w_d;
@@ -327,7 +337,7 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
   g.out = yd;
   g.ldo = c->h;
   g.row_weight = row_weight;
-  e = moe::launch_grouped_gemm_bf16(g, stream, &err);
+  e = launch(g, stream, &err);
   if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "down grouped GEMM launch") : cuda_fail(e, err.c_str());
   counted(2);
   return MOE_OK;

@@ -83,6 +83,8 @@ struct GroupedGemmDesc {
   int* status;
 };
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
+// The expert FFN projections (modes 0 and 1) on CTA pairs: 256 x 256 tiles, tcgen05.mma.cta_group::2.
+cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
 
 // Step 3, FP8 layer: block-scaled grouped GEMM (e4m3 operands, fp32 128x128 weight scales, 1x128
 // activation scales). mode 0: H codes + 1x128 scales; mode 1: yd bf16 x row_weight.

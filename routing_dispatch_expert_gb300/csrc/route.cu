@@ -189,10 +189,11 @@ __device__ __forceinline__ float warp_min(float v) {
 // The selection key of the sigmoid layers is fp32(sigmoid(l)) + bias with the sigmoid evaluated in
 // fp64 and rounded once. The fast pass evaluates it in fp32 (expf, at most 2 ulp, then two correctly
 // rounded operations): |key_fast - key| < 4e-7. A decision taken on the fast keys is the decision on
-// the exact keys whenever every deciding gap exceeds twice the error; the thresholds below are ten
-// times that. A token with a smaller gap is selected again on the exact fp64 keys.
-constexpr float kKeyGap = 4e-6f;    // between two expert keys
-constexpr float kGroupGap = 1e-5f;  // between two group scores (sums of two keys)
+// the exact keys whenever every deciding gap exceeds twice the error (a group score, a sum of two
+// keys, four times it); the thresholds below leave a further margin. A token with a smaller gap is
+// selected again on the exact fp64 keys.
+constexpr float kKeyGap = 1e-6f;    // between two expert keys
+constexpr float kGroupGap = 2e-6f;  // between two group scores (sums of two keys)
 
 __device__ __forceinline__ float sigmoid_exact(float l) { return __double2float_rn(1.0 / (1.0 + exp(-(double)l))); }
 __device__ __forceinline__ float sigmoid_fast(float l) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l))); }
@@ -318,7 +319,22 @@ __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
 
     // route weights
     double w = 0.0;
-    if (!sigmoid) {
+    if (sigmoid) {
+      // w_j = s_j / sum(s) * scale with s = sigmoid(logit) in fp32 (relative error below 4e-7), the
+      // sum of the k scores in fp64; the weights enter the combine, not a selection, so they need no
+      // correctly rounded sigmoid
+      const float sj = lane < d.k ? sigmoid_fast(sel_l) : 0.f;
+      double sum = (double)sj;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const float scale = d.renorm ? __fdiv_rn(d.routed_scale, (float)sum) : d.routed_scale;
+      if (lane < d.k) {
+        d.topk_idx[(int64_t)t * d.k + lane] = sel_e;
+        d.topk_w[(int64_t)t * d.k + lane] = __fmul_rn(sj, scale);
+      }
+      continue;
+    }
+    {
       float lmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
@@ -331,8 +347,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
       if (lane < d.k) w = exp((double)sel_l - (double)lmax) / z;
-    } else {
-      if (lane < d.k) w = (double)sigmoid_exact(sel_l);
     }
     if (d.renorm) {
       double sum = lane < d.k ? w : 0.0;

@@ -11,8 +11,8 @@ import oracle
 import synth
 import routing_dispatch_expert_gb300 as rde
 from routing_dispatch_expert_gb300 import build as pkg_build
-from harness import (BF16_TOL, FP8_TOL, GpuLayer, bits, cfg_of, logit_tolerance, oracle_tokens, rel_err_per_token,
-                     route_kwargs)
+from harness import (BF16_TOL, FP8_TOL, WEIGHT_RTOL, GpuLayer, bits, cfg_of, logit_tolerance, oracle_tokens,
+                     rel_err_per_token, route_kwargs)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def test_full_size_layer(name, n_tok):
     # routing of every token, from the same logits: bit-exact indices
     idx, w = oracle.route(logits, bias, **route_kwargs(wl))
     np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), idx)
-    np.testing.assert_allclose(it["topk_w"].cpu().numpy(), w, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(it["topk_w"].cpu().numpy(), w, rtol=WEIGHT_RTOL, atol=1e-7)
     # aggregation and permutation of every row: bit-exact
     counts, offsets, inv_pos, row_token = oracle.permute(idx, wl.E)
     np.testing.assert_array_equal(it["counts"].cpu().numpy(), counts)
@@ -111,7 +111,7 @@ def test_full_size_fp8_routing_and_dispatch():
     assert rde.device_status(cfg, ws) == 0
     ri, rw = oracle.route(logits.cpu().numpy(), inp["bias"].cpu().numpy(), **route_kwargs(wl))
     np.testing.assert_array_equal(idx.cpu().numpy(), ri)
-    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=WEIGHT_RTOL, atol=1e-7)
     c, off, ip, rt = oracle.permute(ri, E)
     np.testing.assert_array_equal(offsets.cpu().numpy(), off)
     np.testing.assert_array_equal(inv_pos.cpu().numpy(), ip)

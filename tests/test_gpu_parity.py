@@ -8,8 +8,8 @@ import oracle
 import synth
 import routing_dispatch_expert_gb300 as rde
 from routing_dispatch_expert_gb300 import build as pkg_build
-from harness import (BF16_TOL, FP8_TOL, MARGIN, GpuLayer, bits, cfg_of, logit_tolerance, oracle_tokens,
-                     rel_err_per_token, route_kwargs, selection_margin)
+from harness import (BF16_TOL, FP8_TOL, MARGIN, WEIGHT_RTOL, GpuLayer, bits, cfg_of, logit_tolerance,
+                     oracle_tokens, rel_err_per_token, route_kwargs, selection_margin)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,13 @@ SMALL = {
                                           capacity_factor=1.25),
     "cap_mixtral": _W["mixtral"].replace(name="cap_mixtral", T=500, h=512, I=256, capacity_factor=1.0),
     "cap_fp8": _W["dsv3_fp8"].replace(name="cap_fp8", T=200, h=256, E=32, I=128, I_shared=128, capacity_factor=1.1),
+    # at least 1024 rows per expert on average: the bf16 expert GEMMs run on CTA pairs (256-row tiles)
+    "pair_mixtral": _W["mixtral"].replace(name="pair_mixtral", T=4500, h=512, I=384),
+    "pair_dsv3": _W["dsv3_prefill"].replace(name="pair_dsv3", T=2600, h=512, E=8, k=4, n_group=2, topk_group=1,
+                                            I=256, I_shared=256),
+    "fp8_large_groups": _W["dsv3_fp8"].replace(name="fp8_large_groups", T=2200, h=512, E=8, k=4, n_group=2,
+                                               topk_group=1, I=256, I_shared=256),
+    "pair_cap": _W["mixtral"].replace(name="pair_cap", T=4500, h=256, I=256, capacity_factor=1.0),
 }
 
 
@@ -72,7 +79,7 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
     ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, fp8=wl.dtype == "fp8",
                          capacity_factor=wl.capacity_factor, **route_kwargs(wl))
     np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), ref["topk_idx"])
-    np.testing.assert_allclose(it["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(it["topk_w"].cpu().numpy(), ref["topk_w"], rtol=WEIGHT_RTOL, atol=1e-7)
     np.testing.assert_array_equal(it["counts"].cpu().numpy(), ref["counts"])
     np.testing.assert_array_equal(it["offsets"].cpu().numpy(), ref["offsets"])
     np.testing.assert_array_equal(it["inv_pos"].cpu().numpy(), ref["inv_pos"])
@@ -327,21 +334,29 @@ def test_routing_near_ties_bit_exact(score):
     torch.cuda.synchronize()
     ri, rw = oracle.route(logits, bias, **route_kwargs(wl))
     np.testing.assert_array_equal(idx.cpu().numpy(), ri)
-    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=WEIGHT_RTOL, atol=1e-7)
 
 
-@pytest.mark.parametrize("dtype,cf", [("bf16", 0.0), ("fp8", 0.0), ("bf16", 1.1)])
-def test_eplb_placement_matches_unplaced_layer(dtype, cf):
+@pytest.mark.parametrize("dtype,cf,pairs", [("bf16", 0.0, False), ("fp8", 0.0, False), ("bf16", 1.1, False),
+                                            ("bf16", 0.0, True), ("fp8", 0.0, True)])
+def test_eplb_placement_matches_unplaced_layer(dtype, cf, pairs):
     """An EPLB placement (redundant replicas, card-major slots) only reorders the expert-major rows:
-    the per-slot permutation matches the oracle and the layer output is bit-identical."""
-    base = synth.WORKLOADS["dsv3_decode"].replace(T=400, h=512, E=64, I=256, I_shared=256, zipf_s=1.2,
-                                                  dtype=dtype, capacity_factor=cf)
+    the per-slot permutation matches the oracle and the layer output is bit-identical. With `pairs`
+    both layouts average over 1024 rows per slot, so the bf16 layers run the CTA-pair GEMMs."""
+    if pairs:
+        base = synth.WORKLOADS["dsv3_decode"].replace(T=2600, h=512, E=8, k=4, n_group=2, topk_group=1, I=256,
+                                                      I_shared=256, zipf_s=1.2, dtype=dtype, capacity_factor=cf)
+        n_cards, n_redundant = 2, 2
+    else:
+        base = synth.WORKLOADS["dsv3_decode"].replace(T=400, h=512, E=64, I=256, I_shared=256, zipf_s=1.2,
+                                                      dtype=dtype, capacity_factor=cf)
+        n_cards, n_redundant = 8, 8
     L = GpuLayer(base)
     y0 = L.forward().clone()
     it0 = L.intermediates()
     idx = it0["topk_idx"].cpu().numpy()
     load = np.bincount(idx.ravel(), minlength=base.E)
-    plan = rde.eplb_plan(load, n_cards=8, n_redundant=8)
+    plan = rde.eplb_plan(load, n_cards=n_cards, n_redundant=n_redundant)
     pl = rde.Placement(plan)
     cfg = rde.make_config(T=base.T, h=base.h, E=base.E, k=base.k, I=base.I, I_shared=base.I_shared,
                           n_group=base.n_group, topk_group=base.topk_group, score=base.score, renorm=base.renorm,
