@@ -51,25 +51,28 @@ def layer_counts(wl, active_experts):
     return flops, gemm_flops, bytes_
 
 
+GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_fp8.cu", "gemm_common.cuh", "common.cuh")
+
+
 def gemm_source_sha():
     """sha256 over the sources the grouped-GEMM kernels are compiled from."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm_common.cuh", "common.cuh"):
+    for f in GEMM_SOURCES:
         h.update(open(os.path.join(ROOT, "routing_dispatch_expert_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
 
 def gemm_traffic_from_profile(wl):
-    """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it was taken on the
-    current kernel source and this workload; else None."""
+    """DRAM bytes per expert-GEMM launch (mean of the gate/up and down launches) from the committed
+    ncu summary, if it was taken on the current kernel sources and this workload; else None."""
     p = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    sha = gemm_source_sha()
-    if d.get("kernel_source_sha256") != sha or d.get("workload") != wl.name:
+    if d.get("kernel_source_sha256") != gemm_source_sha():
         return None
-    return d.get("dram_bytes_per_launch_full_size")
+    entry = d.get("workloads", {}).get(wl.name)
+    return entry.get("dram_bytes_per_launch") if entry else None
 
 
 class ClockSampler:
