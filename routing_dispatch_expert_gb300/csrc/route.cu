@@ -21,100 +21,76 @@
 namespace moe {
 
 // ------------------------------------------------------------------------------------------
-// router GEMM: logits[T, E] = x[T, h] . w_r[E, h]^T on the CUDA cores in fp32 (bf16 x read
-// directly, converted in registers). 128 x 128 output tile per CTA, 8 x 8 per thread, K step 16,
-// register-staged double buffering.
+// router GEMM for small E (E < 128, or E not a multiple of 32): logits[T, E] = x[T, h] . w_r[E, h]^T
+// on the CUDA cores in fp32. The output is only E columns wide, so the work is split over tokens and K
+// instead of output tiles: a CTA of 8 warps takes TPW tokens and EMAX experts (blockIdx.y selects the
+// expert block when E > 64); warp w takes the 256-element K chunks
+// w, w + 8, ... (each lane 8 consecutive elements of a chunk: one 16-byte load of x per token, two
+// 16-byte loads of each expert's weight row, L1-resident); lanes are summed by a butterfly, the 8
+// warps' partial sums in warp order through shared memory (the same order on every run).
 // ------------------------------------------------------------------------------------------
 namespace rg {
-constexpr int BM = 128, BN = 128, BK = 16, PAD = 4, THREADS = 256;
+constexpr int WARPS = 8, THREADS = 32 * WARPS;
 
-__global__ void __launch_bounds__(THREADS) router_gemm_kernel(const __nv_bfloat16* __restrict__ x,
-                                                              const float* __restrict__ w, float* __restrict__ out,
-                                                              int T, int h, int E) {
-  __shared__ __align__(16) float As[2][BK][BM + PAD];
-  __shared__ __align__(16) float Bs[2][BK][BN + PAD];
-  const int tid = threadIdx.x;
-  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-  const int ty = tid / 16, tx = tid % 16;
-
-  // global -> register staging
-  const int a_row = tid / 2, a_k = (tid % 2) * 8;
-  const bool a_ok = m0 + a_row < T;
-  const __nv_bfloat16* a_src = x + (int64_t)(m0 + a_row) * h + a_k;
-  int b_row[2], b_k[2];
-  bool b_ok[2];
-  const float* b_src[2];
+template <int EMAX, int TPW>
+__global__ void __launch_bounds__(THREADS) router_small_e_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                 const float* __restrict__ w, float* __restrict__ out,
+                                                                 int T, int h, int E) {
+  __shared__ float part[WARPS][TPW][EMAX];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * TPW;
+  const int e0 = blockIdx.y * EMAX;
+  const int ne = min(EMAX, E - e0);  // experts of this block
+  float acc[TPW][EMAX];
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    int idx = tid + THREADS * p;
-    b_row[p] = idx / 4;
-    b_k[p] = (idx % 4) * 4;
-    b_ok[p] = n0 + b_row[p] < E;
-    b_src[p] = w + (int64_t)(n0 + b_row[p]) * h + b_k[p];
+  for (int t = 0; t < TPW; ++t)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[t][e] = 0.f;
+  const int chunks = h / 256;
+  for (int c = warp; c < chunks; c += WARPS) {
+    const int k = c * 256 + lane * 8;
+    float xv[TPW][8];
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) {
+      const uint4 v = t0 + t < T ? *reinterpret_cast<const uint4*>(x + (int64_t)(t0 + t) * h + k)
+                                 : make_uint4(0, 0, 0, 0);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv[t][2 * i] = bf16_lo(u[i]);
+        xv[t][2 * i + 1] = bf16_hi(u[i]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (e < ne) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + (int64_t)(e0 + e) * h + k));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + (int64_t)(e0 + e) * h + k + 4));
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[t][e] = fmaf(xv[t][i], wv[i], acc[t][e]);
+      }
+    }
   }
-  uint4 ra;
-  float4 rb[2];
-  auto load = [&](int k0) {
-    ra = a_ok ? *reinterpret_cast<const uint4*>(a_src + k0) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int p = 0; p < 2; ++p)
-      rb[p] = b_ok[p] ? *reinterpret_cast<const float4*>(b_src[p] + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  auto store = [&](int buf) {
-    const uint32_t av[4] = {ra.x, ra.y, ra.z, ra.w};
+  for (int t = 0; t < TPW; ++t)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      As[buf][a_k + 2 * i][a_row] = bf16_lo(av[i]);
-      As[buf][a_k + 2 * i + 1][a_row] = bf16_hi(av[i]);
+    for (int e = 0; e < EMAX; ++e) {
+      float v = acc[t][e];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) part[warp][t][e] = v;
     }
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      Bs[buf][b_k[p] + 0][b_row[p]] = rb[p].x;
-      Bs[buf][b_k[p] + 1][b_row[p]] = rb[p].y;
-      Bs[buf][b_k[p] + 2][b_row[p]] = rb[p].z;
-      Bs[buf][b_k[p] + 3][b_row[p]] = rb[p].w;
-    }
-  };
-
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  load(0);
-  store(0);
   __syncthreads();
-  int buf = 0;
-  for (int k0 = 0; k0 < h; k0 += BK) {
-    const bool more = k0 + BK < h;
-    if (more) load(k0 + BK);
+  for (int i = threadIdx.x; i < TPW * EMAX; i += THREADS) {
+    const int t = i / EMAX, e = i % EMAX;
+    if (e < ne && t0 + t < T) {
+      float v = part[0][t][e];
 #pragma unroll
-    for (int kk = 0; kk < BK; ++kk) {
-      float a[8], b[8];
-      *reinterpret_cast<float4*>(a) = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-      *reinterpret_cast<float4*>(a + 4) = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
-      *reinterpret_cast<float4*>(b) = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-      *reinterpret_cast<float4*>(b + 4) = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    if (more) {
-      store(buf ^ 1);
-      __syncthreads();
-      buf ^= 1;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    int row = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
-    if (row >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      int col = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
-      if (col < E) out[(int64_t)row * E + col] = acc[i][j];
+      for (int q = 1; q < WARPS; ++q) v += part[q][t][e];
+      out[(int64_t)(t0 + t) * E + e0 + e] = v;
     }
   }
 }
@@ -123,9 +99,19 @@ __global__ void __launch_bounds__(THREADS) router_gemm_kernel(const __nv_bfloat1
 cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, int T, int h, int E,
                                cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  dim3 grid((unsigned)cdiv(T, rg::BM), (unsigned)cdiv(E, rg::BN));
-  rg::router_gemm_kernel<<<grid, rg::THREADS, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(x), w_r, logits,
-                                                            T, h, E);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+#define RG_LAUNCH(EM, TP)                                                                               \
+  rg::router_small_e_kernel<EM, TP>                                                                    \
+      <<<dim3((unsigned)cdiv(T, TP), (unsigned)cdiv(E, EM)), rg::THREADS, 0, stream>>>(xb, w_r, logits, T, h, E)
+  if (E <= 8)
+    RG_LAUNCH(8, 4);
+  else if (E <= 16)
+    RG_LAUNCH(16, 2);
+  else if (E <= 32)
+    RG_LAUNCH(32, 1);
+  else
+    RG_LAUNCH(64, 1);
+#undef RG_LAUNCH
   return cudaGetLastError();
 }
 
