@@ -315,8 +315,8 @@ def main():
     status = rde.device_status(cfg, ws)
     if status != 0:
         raise SystemExit(f"device status {status} after warm-up")
-    counts = rde.ws_view(ws, cfg, "counts", torch.int32, (wl.E,)).cpu().numpy()
-    active = int((counts > 0).sum())
+    bal = rde.balance(cfg, ws)
+    active = bal["active"]
 
     # timed region: K whole-layer steps; the grouped-GEMM pair (moe_expert_ffn) is timed separately
     # on the same stream by running the steps through their own entry points
@@ -451,6 +451,8 @@ def main():
                                "bytes": bytes_, "active_experts": active,
                                "bound": "tensor" if t_compute >= bytes_ / p_hbm else "hbm",
                                "peaks": peaks_kind},
+            "balance": {"max_over_mean": bal["max_over_mean"], "active_experts": bal["active"],
+                        "dropped_assignments": bal["dropped"]},
             "ms_moe_forward": ms_fwd, "ms_expert_ffn": gemm_ms,
             "graph": {"value": job_tokens_per_s(world, wl.T, ms_graph), "unit": UNIT, "ms_per_step": ms_graph,
                       "note": "the same step replayed as one CUDA graph (moe_graph_launch)"},

@@ -245,6 +245,20 @@ def device_status(cfg, ws) -> int:
     return v.value
 
 
+def balance(cfg, ws) -> dict:
+    """Load balance of the last step, read from its workspace (one small device-to-host copy): rows per
+    expert (per physical slot under a placement), busiest / mean (inference guide 6.4, section 5.1:
+    the step waits for the busiest expert), experts with rows, and the assignments a capacity limit
+    dropped."""
+    S = cfg.placement.contents.n_slots if cfg.placement else cfg.E
+    counts = ws_view(ws, cfg, "counts", torch.int32, (S,)).cpu()
+    offsets = ws_view(ws, cfg, "offsets", torch.int32, (S + 1,)).cpu()
+    total = int(offsets[S])
+    mean = total / S if S else 0.0
+    return {"counts": counts.tolist(), "max_over_mean": (int(counts.max()) / mean) if mean > 0 else 0.0,
+            "active": int((counts > 0).sum()), "dropped": cfg.T * cfg.k - total}
+
+
 class MoeLayer:
     """Convenience wrapper: a config, its weights and a workspace; ``layer(x)`` runs moe_forward."""
 

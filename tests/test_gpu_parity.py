@@ -381,3 +381,23 @@ def test_eplb_placement_matches_unplaced_layer(dtype, cf, pairs):
     np.testing.assert_array_equal(row_token[:ro[-1]], rt)
     assert plan["replicas"].max() > 1  # the hot experts really got replicas
     assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+@pytest.mark.parametrize("cf", [0.0, 1.25])
+def test_balance_stats_match_the_oracle_counts(cf):
+    """Per-step balance read back from the workspace: rows per expert, busiest / mean, experts with
+    rows and the assignments a capacity limit dropped, against the oracle's permutation of the same
+    expert indices."""
+    wl = SMALL["cap_skew"].replace(capacity_factor=cf)
+    L = GpuLayer(wl)
+    L.forward()
+    idx = L.intermediates()["topk_idx"].cpu().numpy()
+    b = rde.balance(L.cfg, L.ws)
+    cap = oracle.capacity(cf, wl.T, wl.k, wl.E)
+    counts, offsets, _, _ = oracle.permute_capacity(idx, wl.E, cap)
+    assert b["counts"] == counts.tolist()
+    assert b["dropped"] == wl.T * wl.k - int(offsets[-1])
+    assert b["active"] == int((counts > 0).sum())
+    assert b["max_over_mean"] == pytest.approx(counts.max() / (offsets[-1] / wl.E), rel=1e-12)
+    if cf > 0:
+        assert b["dropped"] > 0 and max(b["counts"]) <= cap  # the skewed router really overflows
