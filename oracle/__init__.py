@@ -60,6 +60,13 @@ def lib():
             L.orc_bf16_to_double_n.argtypes = [vp, i64, vp]
             L.orc_e4m3_encode_n.argtypes = [vp, i64, vp]
             L.orc_e4m3_decode_n.argtypes = [vp, i64, vp]
+            L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e2m1_decode.restype = ctypes.c_double
+            L.orc_e2m1_encode.argtypes = [f32]
+            L.orc_e2m1_encode.restype = ctypes.c_uint8
+            L.orc_quant_weight_nvfp4.argtypes = [vp, i64, i64, vp, vp, vp]
+            L.orc_dequant_nvfp4.argtypes = [vp, vp, f32, i64, i64, vp]
+            L.orc_expert_ffn_nvfp4.argtypes = [vp, i64, i64, i64, vp, vp, f32, vp, vp, f32, vp]
             _lib = L
     return _lib
 
@@ -121,6 +128,39 @@ def quant_weight_128x128(w_bf16) -> tuple[np.ndarray, np.ndarray]:
     s = np.empty((r // 128, c // 128), np.float32)
     lib().orc_quant_weight_128x128(_p(w), r, c, _p(q), _p(s))
     return q, s
+
+
+def e2m1_decode(c) -> np.ndarray:
+    """values of 4-bit e2m1 codes (low nibble)"""
+    c = np.asarray(c, np.uint8)
+    return np.array([lib().orc_e2m1_decode(int(v)) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def e2m1_encode(f) -> np.ndarray:
+    """nearest e2m1 codes of fp32 values (ties to the even code, saturating at 6)"""
+    f = np.asarray(f, np.float32)
+    return np.array([lib().orc_e2m1_encode(float(v)) for v in f.ravel()], np.uint8).reshape(f.shape)
+
+
+def quant_weight_nvfp4(w_bf16) -> tuple[np.ndarray, np.ndarray, float]:
+    """NVFP4 quantisation of a [rows, cols] bf16 matrix -> (codes [rows, cols/2] two per byte, e4m3
+    block scales [rows, cols/16], fp32 matrix scale)"""
+    w = _c(w_bf16, np.uint16)
+    r, c = w.shape
+    assert c % 16 == 0
+    q = np.empty((r, c // 2), np.uint8)
+    sc = np.empty((r, c // 16), np.uint8)
+    g = np.zeros(1, np.float32)
+    lib().orc_quant_weight_nvfp4(_p(w), r, c, _p(q), _p(sc), _p(g))
+    return q, sc, float(g[0])
+
+
+def dequant_nvfp4(q, sc, g) -> np.ndarray:
+    q, sc = _c(q, np.uint8), _c(sc, np.uint8)
+    r, c2 = q.shape
+    out = np.empty((r, 2 * c2), np.float64)
+    lib().orc_dequant_nvfp4(_p(q), _p(sc), float(g), r, 2 * c2, _p(out))
+    return out
 
 
 # ---------------------------------------------------------------- step 1: route
@@ -219,6 +259,20 @@ def expert_ffn_fp8(xq, xs, w_gu_q, w_gu_s, w_d_q, w_d_s) -> np.ndarray:
     return out
 
 
+def expert_ffn_nvfp4(x_bf16, w_gu, w_d) -> np.ndarray:
+    """bf16 rows through one expert whose matrices are NVFP4 tuples (codes, scales, matrix scale)"""
+    x = _c(x_bf16, np.uint16)
+    (gq, gsc, gg), (dq, dsc, dg) = w_gu, w_d
+    gq, gsc, dq, dsc = _c(gq, np.uint8), _c(gsc, np.uint8), _c(dq, np.uint8), _c(dsc, np.uint8)
+    m, h = x.shape
+    I = 2 * dq.shape[1]
+    assert gq.shape == (2 * I, h // 2) and dq.shape == (h, I // 2)
+    out = np.empty((m, h), np.float64)
+    if m:
+        lib().orc_expert_ffn_nvfp4(_p(x), m, h, I, _p(gq), _p(gsc), float(gg), _p(dq), _p(dsc), float(dg), _p(out))
+    return out
+
+
 # ---------------------------------------------------------------- step 4: combine
 def combine(o, w, shared=None) -> np.ndarray:
     """o [n, k, h] fp64 expert outputs per (token, slot); w [n, k]; shared [n, h] or None -> y bf16 [n, h]"""
@@ -313,11 +367,12 @@ def imbalance(counts, n_cards) -> float:
 
 # ---------------------------------------------------------------- whole layer (small shapes)
 def forward(x_bf16, w_r, bias, experts, shared, *, k, n_group=1, topk_group=1, score=SOFTMAX, renorm=False,
-            routed_scale=1.0, fp8=False, logits=None, capacity_factor=0.0):
+            routed_scale=1.0, fp8=False, nvfp4=False, logits=None, capacity_factor=0.0):
     """The whole layer for shapes the oracle finishes in seconds.
 
     experts: list of (w_gu [2I, h], w_d [h, I]) bf16 per routed expert; shared: same tuple or None.
-    FP8 layers quantise the expert weights 128x128 and the activations 1x128 first.
+    FP8 layers quantise the expert weights 128x128 and the activations 1x128 first; NVFP4 layers
+    quantise the expert weights to NVFP4 and keep the activations bf16.
     logits: router logits to route on (default: computed here from x and w_r).
     Returns a dict with every intermediate of the path.
     """
@@ -349,6 +404,16 @@ def forward(x_bf16, w_r, bias, experts, shared, *, k, n_group=1, topk_group=1, s
         if shared is not None:
             (gq, gs), (dq, ds) = quant_weight_128x128(shared[0]), quant_weight_128x128(shared[1])
             sh = expert_ffn_fp8(xq, xs, gq, gs, dq, ds)
+    elif nvfp4:
+        xd = gather_rows(x, row_token)
+        out.update(xd=xd)
+        q = lambda pair: (quant_weight_nvfp4(pair[0]), quant_weight_nvfp4(pair[1]))  # noqa: E731
+        o_rows = np.empty((R, h), np.float64)
+        for e in range(E):
+            a, b = offsets[e], offsets[e + 1]
+            if b > a:
+                o_rows[a:b] = expert_ffn_nvfp4(xd[a:b], *q(experts[e]))
+        sh = None if shared is None else expert_ffn_nvfp4(x, *q(shared))
     else:
         xd = gather_rows(x, row_token)
         out.update(xd=xd)

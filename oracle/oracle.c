@@ -37,6 +37,14 @@
  *   R8 storage points: the SwiGLU product is stored in bf16 (FP8 1x128 in the FP8 layer);
  *   R10 FP8 scale = amax / 448 in fp32, all-zero block -> scale 1, round-to-nearest-even with
  *       saturation to +-448.
+ *   R19 FP4 expert weights ([TRTLLM] "Precision strategy": the MoE weights of the Blackwell
+ *       deployment are FP4, halving the weight bytes a memory-bound decode step streams) use
+ *       the NVFP4 layout: e2m1 elements, one e4m3 scale per 16 consecutive elements of a row,
+ *       one fp32 scale per weight matrix; activations stay bf16 (weight-only FP4);
+ *   R20 NVFP4 quantisation: global g = amax(W) / (6 * 448) in fp32 (all-zero matrix -> 1);
+ *       block code s = e4m3(fp32(amax_block / fp32(6 * g))); element code e2m1(fp32(w /
+ *       fp32(s * g))), nearest with ties to the even code, saturating at +-6; a block whose
+ *       scale code is zero has all element codes zero. Value = e2m1 * s * g.
  */
 #include <math.h>
 #include <stdint.h>
@@ -169,6 +177,82 @@ ORC_API void orc_quant_weight_128x128(const uint16_t* w, int64_t rows, int64_t c
           q[o] = orc_e4m3_encode((float)(orc_bf16_to_double(w[o]) / (double)sc));
         }
     }
+}
+
+/* ------------------------------------------------------------------------------------------
+ * FP4 e2m1 (OCP Microscaling formats, the element type of NVFP4; reading R19): 1 sign, 2
+ * exponent bits with bias 1, 1 mantissa bit; exponent field 0 is subnormal; no infinities or
+ * NaN. Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. A code is the low nibble of a byte.
+ * ---------------------------------------------------------------------------------------- */
+ORC_API double orc_e2m1_decode(uint8_t c) {
+  int s = (c >> 3) & 1, E = (c >> 1) & 3, M = c & 1;
+  double v = E == 0 ? 0.5 * M : ldexp(1.0 + 0.5 * M, E - 1);
+  return s ? -v : v;
+}
+
+/* Nearest e2m1 value to f, ties to the even code (mantissa bit 0), magnitudes above 6 saturate
+ * to 6, NaN -> +0 (the format has no NaN). Positive codes 0..7 are monotone in value. */
+ORC_API uint8_t orc_e2m1_encode(float f) {
+  if (isnan(f)) return 0;
+  uint8_t sign = signbit(f) ? 0x8 : 0x0;
+  double a = fabs((double)f);
+  if (a >= 6.0) return sign | 0x7;
+  int lo = 0;
+  while (lo < 7 && orc_e2m1_decode((uint8_t)(lo + 1)) <= a) ++lo;
+  int code = lo;
+  if (lo < 7) {
+    double vlo = orc_e2m1_decode((uint8_t)lo), vhi = orc_e2m1_decode((uint8_t)(lo + 1));
+    if (a - vlo > vhi - a || (a - vlo == vhi - a && (lo & 1))) code = lo + 1;
+  }
+  return sign | (uint8_t)code;
+}
+
+/* NVFP4 quantisation of one weight matrix (readings R19, R20). w: [rows, cols] bf16 with
+ * cols % 16 == 0. q: [rows, cols / 2] bytes, element 2i in the low nibble of byte i, 2i + 1 in
+ * the high nibble; s: [rows, cols / 16] e4m3 block-scale codes; *g: the fp32 matrix scale. */
+ORC_API void orc_quant_weight_nvfp4(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* s,
+                                    float* g) {
+  double amax = 0.0;
+  for (int64_t i = 0; i < rows * cols; ++i) {
+    double a = fabs(orc_bf16_to_double(w[i]));
+    if (a > amax) amax = a;
+  }
+  const float gs = amax == 0.0 ? 1.0f : (float)(amax / 2688.0);
+  const float d = (float)(6.0 * (double)gs);
+  *g = gs;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < cols / 16; ++b) {
+      const uint16_t* blk = w + r * cols + b * 16;
+      double bmax = 0.0;
+      for (int i = 0; i < 16; ++i) {
+        double a = fabs(orc_bf16_to_double(blk[i]));
+        if (a > bmax) bmax = a;
+      }
+      const uint8_t sc = orc_e4m3_encode((float)(bmax / (double)d));
+      s[r * (cols / 16) + b] = sc;
+      const float p = (float)(orc_e4m3_decode(sc) * (double)gs);
+      for (int i = 0; i < 16; i += 2) {
+        uint8_t c0 = 0, c1 = 0;
+        if (p != 0.0f) {
+          c0 = orc_e2m1_encode((float)(orc_bf16_to_double(blk[i]) / (double)p));
+          c1 = orc_e2m1_encode((float)(orc_bf16_to_double(blk[i + 1]) / (double)p));
+        }
+        q[r * (cols / 2) + b * 8 + i / 2] = (uint8_t)(c0 | (c1 << 4));
+      }
+    }
+}
+
+/* Value of element (r, c) of an NVFP4 matrix: e2m1 * e4m3 block scale * matrix scale. */
+static double orc_nvfp4_value(const uint8_t* q, const uint8_t* s, float g, int64_t cols, int64_t r, int64_t c) {
+  uint8_t byte = q[r * (cols / 2) + c / 2];
+  uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+  return orc_e2m1_decode(code) * orc_e4m3_decode(s[r * (cols / 16) + c / 16]) * (double)g;
+}
+
+ORC_API void orc_dequant_nvfp4(const uint8_t* q, const uint8_t* s, float g, int64_t rows, int64_t cols, double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) out[r * cols + c] = orc_nvfp4_value(q, s, g, cols, r, c);
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -426,6 +510,34 @@ ORC_API void orc_expert_ffn_fp8(const uint8_t* xq, const float* xs, int64_t m, i
   free(a);
   free(aq);
   free(as);
+}
+
+/* NVFP4-weight variant (readings R19, R20): bf16 activations, weights given as NVFP4 matrices
+ * w_gu: [2I, h] (codes [2I, h/2], scales [2I, h/16], matrix scale g_gu) and w_d: [h, I]; the
+ * SwiGLU product is stored in bf16 as in the bf16 layer (R8). */
+ORC_API void orc_expert_ffn_nvfp4(const uint16_t* x, int64_t m, int64_t h, int64_t I, const uint8_t* w_gu_q,
+                                  const uint8_t* w_gu_s, float g_gu, const uint8_t* w_d_q, const uint8_t* w_d_s,
+                                  float g_d, double* out) {
+  double* a = (double*)malloc(sizeof(double) * I);
+  for (int64_t r = 0; r < m; ++r) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < I; ++c) {
+      double g = 0.0, u = 0.0;
+      for (int64_t d = 0; d < h; ++d) {
+        double xv = orc_bf16_to_double(x[r * h + d]);
+        g += xv * orc_nvfp4_value(w_gu_q, w_gu_s, g_gu, h, c, d);
+        u += xv * orc_nvfp4_value(w_gu_q, w_gu_s, g_gu, h, I + c, d);
+      }
+      a[c] = orc_bf16_to_double(orc_bf16_from_double(orc_silu(g) * u));
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t d = 0; d < h; ++d) {
+      double o = 0.0;
+      for (int64_t c = 0; c < I; ++c) o += a[c] * orc_nvfp4_value(w_d_q, w_d_s, g_d, I, d, c);
+      out[r * h + d] = o;
+    }
+  }
+  free(a);
 }
 
 /* ------------------------------------------------------------------------------------------

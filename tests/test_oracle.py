@@ -313,6 +313,109 @@ def test_expert_ffn_fp8_matches_torch_dequantised():
     assert np.abs(ours - ref).max() <= 1e-4 * np.abs(ref).max()
 
 
+# ------------------------------------------------------------------------------------ NVFP4 (e2m1)
+# OCP Microscaling formats specification, FP4 E2M1 element: the 8 magnitudes of codes 0..7
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_all_codes_match_the_format_table():
+    for c in range(16):
+        v = float(oracle.e2m1_decode(c))
+        assert v == (-1.0 if c & 8 else 1.0) * E2M1_TABLE[c & 7]
+        assert math.copysign(1.0, v) == (-1.0 if c & 8 else 1.0)  # -0 keeps its sign
+
+
+def test_e2m1_encode_is_nearest_with_ties_to_even_code():
+    # brute force: argmin distance over the table, ties to the code whose mantissa bit is 0
+    def ref(f):
+        a = min(abs(f), 6.0)
+        d = [abs(a - v) for v in E2M1_TABLE]
+        best = min(d)
+        cands = [c for c in range(8) if d[c] == best]
+        code = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+        return code | (8 if math.copysign(1.0, f) < 0 else 0)
+
+    rng = np.random.default_rng(21)
+    xs = np.concatenate([np.linspace(-8, 8, 3201), rng.standard_normal(2000) * 3,
+                         [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, 6.0, 1e9, -1e9, 0.0, -0.0]])
+    xs = xs.astype(np.float32)
+    ours = oracle.e2m1_encode(xs)
+    want = np.array([ref(float(f)) for f in xs], np.uint8)
+    np.testing.assert_array_equal(ours, want)
+
+
+def _nvfp4_gap(a):
+    """spacing of the e2m1 grid around magnitude a (in units of the block's value scale)"""
+    return np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+
+
+def test_quant_weight_nvfp4_error_bound_block_max_and_packing():
+    rng = np.random.default_rng(22)
+    rows, cols = 64, 256
+    w = oracle.bf16_from_double(rng.standard_normal((rows, cols)) * 0.02 * np.exp(rng.standard_normal((rows, 1))))
+    wv = oracle.bf16_to_double(w)
+    q, sc, g = oracle.quant_weight_nvfp4(w)
+    amax = np.abs(wv).max()
+    assert g == float(np.float32(amax) / np.float32(2688.0))  # the matrix maps onto 6 x 448
+    deq = oracle.dequant_nvfp4(q, sc, g)
+    p = (oracle.e4m3_decode(sc) * g).repeat(16, axis=1)  # value of one e2m1 step 1.0, per element
+    # round to nearest on the e2m1 grid: within half a grid step (saturation at 6 included: the
+    # block scale is rounded to e4m3, at most 1/16 relative, so a block max lands in [5.6, 6.4])
+    err = np.abs(deq - wv)
+    assert np.all(err <= p * _nvfp4_gap(np.abs(wv) / p) / 2 * (1 + 1e-6) + 1e-30)
+    # the largest element of every block with a normal (not subnormal) e4m3 scale sits at the top of
+    # the grid: code magnitude 7 (value 6)
+    codes = np.empty((rows, cols), np.uint8)
+    codes[:, 0::2] = q & 15
+    codes[:, 1::2] = q >> 4
+    blk = np.abs(wv).reshape(rows, cols // 16, 16).argmax(axis=2)
+    top = np.take_along_axis(codes.reshape(rows, cols // 16, 16), blk[..., None], axis=2)[..., 0]
+    normal = ((sc >> 3) & 15) > 0
+    assert normal.mean() > 0.9 and np.all((top[normal] & 7) == 7)
+    # element 2i is the low nibble: a single nonzero element 1 lands in the high nibble of byte 0
+    one = np.zeros((1, 16), np.uint16)
+    one[0, 1] = oracle.bf16_from_double(np.array([0.5]))[0]
+    q1, s1, g1 = oracle.quant_weight_nvfp4(one)
+    assert q1[0, 0] == 0x70 and np.all(q1[0, 1:] == 0)
+    assert float(oracle.dequant_nvfp4(q1, s1, g1)[0, 1]) == pytest.approx(0.5, rel=1e-6)
+
+
+def test_quant_weight_nvfp4_zero_matrix_and_zero_block():
+    q, sc, g = oracle.quant_weight_nvfp4(np.zeros((4, 32), np.uint16))
+    assert g == 1.0 and np.all(q == 0) and np.all(sc == 0)
+    w = np.zeros((2, 32), np.uint16)
+    w[:, 16:] = oracle.bf16_from_double(np.linspace(-1, 1, 32).reshape(2, 16))
+    q, sc, g = oracle.quant_weight_nvfp4(w)
+    assert np.all(sc[:, 0] == 0) and np.all(q[:, :8] == 0) and np.all(sc[:, 1] != 0)
+
+
+def test_quant_weight_nvfp4_grid_values_round_trip():
+    # a matrix whose entries are e2m1 grid values times a power of two (each block holding a 6)
+    rng = np.random.default_rng(23)
+    v = np.array(E2M1_TABLE)[rng.integers(0, 8, (8, 64))] * np.where(rng.random((8, 64)) < 0.5, -1, 1)
+    v[:, ::16] = 6.0
+    w = oracle.bf16_from_double(v * 2.0 ** -5)
+    q, sc, g = oracle.quant_weight_nvfp4(w)
+    np.testing.assert_allclose(oracle.dequant_nvfp4(q, sc, g), v * 2.0 ** -5, rtol=1e-6, atol=0)
+
+
+def test_expert_ffn_nvfp4_matches_torch_swiglu_on_dequantised_weights():
+    rng = np.random.default_rng(24)
+    m, h, I = 7, 256, 128
+    x = oracle.bf16_from_double(rng.standard_normal((m, h)))
+    w_gu = oracle.bf16_from_double(rng.standard_normal((2 * I, h)) * 0.02)
+    w_d = oracle.bf16_from_double(rng.standard_normal((h, I)) * 0.02)
+    gu4, d4 = oracle.quant_weight_nvfp4(w_gu), oracle.quant_weight_nvfp4(w_d)
+    ours = oracle.expert_ffn_nvfp4(x, gu4, d4)
+    xs = torch.from_numpy(oracle.bf16_to_double(x))
+    wg = torch.from_numpy(oracle.dequant_nvfp4(*gu4))
+    wd = torch.from_numpy(oracle.dequant_nvfp4(*d4))
+    a = torch.nn.functional.silu(xs @ wg[:I].T) * (xs @ wg[I:].T)
+    a = a.to(torch.bfloat16).to(torch.float64)  # the SwiGLU product is stored in bf16
+    ref = (a @ wd.T).numpy()
+    assert np.abs(ours - ref).max() <= 1e-6 * np.abs(ref).max()
+
+
 # ------------------------------------------------------------------------------------ combine
 def test_combine_identity_experts_closed_form():
     """Identity experts: y = x * sum_j w_j (+ x with an identity shared expert)."""
