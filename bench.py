@@ -38,11 +38,27 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def weight_bytes(wl):
+    """bytes per expert-weight element: bf16 2; e4m3 1 (+ 4 / 128^2 of fp32 scales); NVFP4 1/2 + 1/16
+    (an e4m3 scale per 16 elements)"""
+    return {"bf16": 2.0, "fp8": 1.0 + 4.0 / 16384, "nvfp4": 0.5 + 1.0 / 16}[wl.dtype]
+
+
+def gemm_bytes(wl, active_experts):
+    """Algorithmic bytes of the expert-GEMM pair of one step: the weights of the experts with rows (and
+    the shared expert's) read once, the expert-major rows read, the SwiGLU product written and read
+    back, the route-weighted rows written."""
+    R_tot = wl.T * wl.k + (wl.T if wl.has_shared else 0)
+    act = 1.0 if wl.dtype == "fp8" else 2.0
+    w = (active_experts * 3.0 * wl.h * wl.I + 3.0 * wl.h * wl.I_shared) * weight_bytes(wl)
+    return w + R_tot * (wl.h * act + 2.0 * wl.I * act + 2.0 * wl.h)
+
+
 def layer_counts(wl, active_experts):
     """Algorithmic FLOPs and bytes of one layer step (inputs, outputs and the weights that must be
     read; the permute buffers are overhead, not algorithmic)."""
     T, h, E, k, I, Is = wl.T, wl.h, wl.E, wl.k, wl.I, wl.I_shared
-    wbytes = 1 if wl.dtype == "fp8" else 2
+    wbytes = weight_bytes(wl)
     gemm_flops = 6.0 * T * k * h * I + 6.0 * T * h * Is
     flops = 2.0 * T * h * E + gemm_flops
     bytes_ = (2.0 * T * h * 2  # x in, y out (bf16)
@@ -165,6 +181,11 @@ def time_cpu_oracle(wl, budget_s):
                 sq, ss = oracle.quant_1x128(oracle.bf16_to_double(x))
                 (a, b), (c, d) = oracle.quant_weight_128x128(sh[0]), oracle.quant_weight_128x128(sh[1])
                 shared = oracle.expert_ffn_fp8(sq, ss, a, b, c, d)
+        elif wl.dtype == "nvfp4":
+            o_rows = oracle.expert_ffn_nvfp4(xd, oracle.quant_weight_nvfp4(gu0), oracle.quant_weight_nvfp4(d0))
+            shared = None
+            if sh is not None:
+                shared = oracle.expert_ffn_nvfp4(x, oracle.quant_weight_nvfp4(sh[0]), oracle.quant_weight_nvfp4(sh[1]))
         else:
             o_rows = oracle.expert_ffn_bf16(xd, gu0, d0)
             shared = oracle.expert_ffn_bf16(x, sh[0], sh[1]) if sh is not None else None
@@ -301,6 +322,10 @@ def main():
             wts["w_gu_shared"], wts["s_gu_shared"] = rde.quantize_weights_fp8(inp["w_gu_shared"])
             wts["w_d_shared"], wts["s_d_shared"] = rde.quantize_weights_fp8(inp["w_d_shared"])
         del inp["w_gu"], inp["w_d"]
+    elif wl.dtype == "nvfp4":
+        for n in ("gu", "d") + (("gu_shared", "d_shared") if wl.has_shared else ()):
+            wts["w_" + n], wts["s_" + n], wts["g_" + n] = rde.quantize_weights_nvfp4(inp["w_" + n])
+        del inp["w_gu"], inp["w_d"]
     weights = rde.Weights(w_router=inp["w_router"], bias=inp["bias"], **wts)
     ws = rde.alloc_workspace(cfg, dev)
     rde.device_status(cfg, ws)
@@ -426,6 +451,29 @@ def main():
     gemm_peak = peaks["bf16_tflops"] * ratio
     gemm_peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
     traffic = gemm_traffic_from_profile(wl)
+    hbm_bound = t_compute < bytes_ / p_hbm
+    if wl.dtype == "fp8":
+        gemm_kernel = "grouped_gemm_fp8_kernel"
+    elif wl.dtype == "nvfp4":
+        gemm_kernel = "grouped_gemm_nvfp4_kernel"
+    elif wl.T * wl.k >= 1024 * wl.E:
+        gemm_kernel = "grouped_gemm_bf16_pair_kernel"
+    else:
+        gemm_kernel = "grouped_gemm_bf16_kernel"
+    if hbm_bound:
+        # a weight-streaming step: the expert GEMMs against the measured copy bandwidth
+        gb = gemm_bytes(wl, active)
+        roof = {"bound": "hbm", "achieved": gb / (gemm_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gb / (gemm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": traffic, "algorithmic_bytes": gb,
+                "kernel": gemm_kernel + " (gate/up + down launches of one step)",
+                "peak_kind": f"HBM copy bandwidth, {peaks_kind}", "tflops": gemm_tflops}
+    else:
+        roof = {"bound": "tensor", "achieved": gemm_tflops, "peak": gemm_peak, "unit": "TFLOP/s",
+                "frac": gemm_tflops / gemm_peak, "traffic": traffic,
+                "kernel": gemm_kernel + " (gate/up + down launches of one step)",
+                "peak_kind": (f"fp8 = 2 x bf16 burst ({peaks_kind}), nominal ratio" if wl.dtype == "fp8"
+                              else f"bf16 burst, {peaks_kind}"),
+                "frac_of_sustained": gemm_tflops / gemm_peak_sus}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -440,16 +488,10 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if wl.dtype == "fp8" else "bf16",
             "data": "synthetic", "config": config_of(wl, world),
-            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": gemm_peak, "unit": "TFLOP/s",
-                         "frac": gemm_tflops / gemm_peak, "traffic": traffic,
-                         "kernel": ("grouped_gemm_fp8_kernel" if wl.dtype == "fp8" else "grouped_gemm_bf16_kernel")
-                                   + " (gate/up + down launches of one step)",
-                         "peak_kind": (f"fp8 = 2 x bf16 burst ({peaks_kind}), nominal ratio" if wl.dtype == "fp8"
-                                       else f"bf16 burst, {peaks_kind}"),
-                         "frac_of_sustained": gemm_tflops / gemm_peak_sus},
+            "roofline": roof,
             "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3), "flops": flops,
                                "bytes": bytes_, "active_experts": active,
-                               "bound": "tensor" if t_compute >= bytes_ / p_hbm else "hbm",
+                               "bound": "hbm" if hbm_bound else "tensor",
                                "peaks": peaks_kind},
             "balance": {"max_over_mean": bal["max_over_mean"], "active_experts": bal["active"],
                         "dropped_assignments": bal["dropped"]},

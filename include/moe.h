@@ -56,6 +56,10 @@ typedef struct CUstream_st* moe_stream_t; /* the same handle type as cudaStream_
 /* expert arithmetic (moe_config.dtype) */
 #define MOE_DTYPE_BF16 0          /* bf16 operands, fp32 accumulation */
 #define MOE_DTYPE_FP8_BLOCK128 1  /* e4m3 operands; weights 128x128 fp32 scales, activations 1x128 */
+#define MOE_DTYPE_NVFP4 2         /* NVFP4 expert weights (e2m1, e4m3 scale per 16, fp32 per matrix), bf16
+                                     activations, fp32 accumulation (TensorRT-LLM "DeepSeek R1 throughput on
+                                     Blackwell", "Precision strategy": FP4 MoE weights). h and I must be
+                                     multiples of 256 */
 
 /* moe_route flags */
 #define MOE_LOGITS_GIVEN 1 /* `logits` is an input: skip the router GEMM */
@@ -90,7 +94,7 @@ typedef struct {
   int32_t score;        /* MOE_SCORE_SOFTMAX | MOE_SCORE_SIGMOID */
   int32_t renormalize;  /* 1: divide the selected weights by their sum */
   float routed_scale;   /* multiplies the routed weights (DeepSeek-V3: 2.5) */
-  int32_t dtype;        /* MOE_DTYPE_BF16 | MOE_DTYPE_FP8_BLOCK128 */
+  int32_t dtype;        /* MOE_DTYPE_BF16 | MOE_DTYPE_FP8_BLOCK128 | MOE_DTYPE_NVFP4 */
   float capacity_factor;/* 0: dropless. > 0: every expert keeps at most ceil(capacity_factor * T * k / E)
                            assignments, the earliest tokens first; the rest skip that expert (Ultralytics
                            "Load balancing and capacity": a capacity factor such as 1.25x the fair
@@ -99,17 +103,26 @@ typedef struct {
                            counts and offsets are per physical slot (n_slots of them) in slot order */
 } moe_config;
 
+/* Expert matrices are row-major [rows, cols] with cols the reduction (K) dimension. NVFP4 matrices
+ * (MOE_DTYPE_NVFP4, as written by moe_quantize_weights_nvfp4) are three arrays: codes [rows, cols/2]
+ * bytes (element 2i in the low nibble of byte i, 2i+1 in the high nibble), block scales [rows, cols/16]
+ * e4m3 bytes (passed through the s_* pointers), and one fp32 matrix scale (g_*); element value =
+ * e2m1 * e4m3 * matrix scale. */
 typedef struct {
   const float* w_router;   /* [E, h] fp32 router weight (no router bias) */
   const float* bias;       /* [E] fp32 selection bias (sigmoid scoring only), or NULL */
-  const void* w_gu;        /* [E, 2I, h]: rows [0, I) gate, rows [I, 2I) up; bf16 or e4m3 */
-  const float* s_gu;       /* FP8 only: [E, 2I/128, h/128] fp32 block scales */
-  const void* w_d;         /* [E, h, I] down projection; bf16 or e4m3 */
-  const float* s_d;        /* FP8 only: [E, h/128, I/128] */
+  const void* w_gu;        /* [E, 2I, h]: rows [0, I) gate, rows [I, 2I) up; bf16, e4m3 or NVFP4 codes */
+  const float* s_gu;       /* FP8: [E, 2I/128, h/128] fp32 block scales; NVFP4: [E, 2I, h/16] e4m3 bytes */
+  const void* w_d;         /* [E, h, I] down projection; bf16, e4m3 or NVFP4 codes */
+  const float* s_d;        /* FP8: [E, h/128, I/128]; NVFP4: [E, h, I/16] e4m3 bytes */
   const void* w_gu_shared; /* [2I, h] shared expert gate/up, or NULL when I_shared == 0 */
-  const float* s_gu_shared;/* FP8 only: [2I/128, h/128] */
+  const float* s_gu_shared;/* FP8: [2I/128, h/128]; NVFP4: [2I, h/16] */
   const void* w_d_shared;  /* [h, I] shared expert down */
-  const float* s_d_shared; /* FP8 only: [h/128, I/128] */
+  const float* s_d_shared; /* FP8: [h/128, I/128]; NVFP4: [h, I/16] */
+  const float* g_gu;       /* NVFP4 only: [E] fp32 matrix scales of w_gu */
+  const float* g_d;        /* NVFP4 only: [E] fp32 matrix scales of w_d */
+  const float* g_gu_shared;/* NVFP4 only: [1] */
+  const float* g_d_shared; /* NVFP4 only: [1] */
 } moe_weights;
 
 /* Byte offsets of the intermediates inside a moe_forward workspace (all 256-byte aligned).
@@ -250,6 +263,17 @@ int moe_graph_destroy(moe_graph graph);
  * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 int moe_quantize_weights_fp8(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, float* s,
                              moe_stream_t stream);
+
+/* NVFP4 weight quantisation for MOE_DTYPE_NVFP4 layers (TensorRT-LLM "DeepSeek R1 throughput on
+ * Blackwell", "Precision strategy": the MoE weights are FP4; the page does not fix the format, this
+ * is the NVFP4 layout). For each of `batch` row-major [rows, cols] bf16 matrices: matrix scale g =
+ * amax / (6 * 448) in fp32 (1 for an all-zero matrix); per 16 consecutive elements of a row, block
+ * scale s = e4m3(amax_block / (6 g)) and codes e2m1(w / (s g)), nearest even with saturation (all zero
+ * when s is zero). w [batch, rows, cols] bf16 in; q [batch, rows, cols/2] codes, s [batch, rows, cols/16]
+ * e4m3 bytes and g [batch] fp32 out. cols must be a multiple of 256.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+int moe_quantize_weights_nvfp4(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, void* s,
+                               float* g, moe_stream_t stream);
 
 /* EPLB placement plan (inference guide 6.4, sections 5.2-5.3), on the host: n_redundant extra replicas
  * go one by one to the expert with the largest load per replica (first expert on ties); then every

@@ -191,9 +191,10 @@ ORC_API double orc_e2m1_decode(uint8_t c) {
 }
 
 /* Nearest e2m1 value to f, ties to the even code (mantissa bit 0), magnitudes above 6 saturate
- * to 6, NaN -> +0 (the format has no NaN). Positive codes 0..7 are monotone in value. */
+ * to 6; the format has no NaN, and NaN maps to +6 like an overflow. Positive codes 0..7 are
+ * monotone in value. */
 ORC_API uint8_t orc_e2m1_encode(float f) {
-  if (isnan(f)) return 0;
+  if (isnan(f)) return 0x7;
   uint8_t sign = signbit(f) ? 0x8 : 0x0;
   double a = fabs((double)f);
   if (a >= 6.0) return sign | 0x7;
@@ -213,6 +214,7 @@ ORC_API uint8_t orc_e2m1_encode(float f) {
 ORC_API void orc_quant_weight_nvfp4(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* q, uint8_t* s,
                                     float* g) {
   double amax = 0.0;
+#pragma omp parallel for schedule(static) reduction(max : amax)
   for (int64_t i = 0; i < rows * cols; ++i) {
     double a = fabs(orc_bf16_to_double(w[i]));
     if (a > amax) amax = a;
@@ -514,29 +516,40 @@ ORC_API void orc_expert_ffn_fp8(const uint8_t* xq, const float* xs, int64_t m, i
 
 /* NVFP4-weight variant (readings R19, R20): bf16 activations, weights given as NVFP4 matrices
  * w_gu: [2I, h] (codes [2I, h/2], scales [2I, h/16], matrix scale g_gu) and w_d: [h, I]; the
- * SwiGLU product is stored in bf16 as in the bf16 layer (R8). */
+ * weights are dequantised to fp64 first (exact), then the SwiGLU FFN runs as in the bf16 layer,
+ * with the product stored in bf16 (R8). */
 ORC_API void orc_expert_ffn_nvfp4(const uint16_t* x, int64_t m, int64_t h, int64_t I, const uint8_t* w_gu_q,
                                   const uint8_t* w_gu_s, float g_gu, const uint8_t* w_d_q, const uint8_t* w_d_s,
                                   float g_d, double* out) {
+  double* gu = (double*)malloc(sizeof(double) * 2 * I * h);
+  double* wd = (double*)malloc(sizeof(double) * h * I);
   double* a = (double*)malloc(sizeof(double) * I);
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < 2 * I; ++r)
+    for (int64_t c = 0; c < h; ++c) gu[r * h + c] = orc_nvfp4_value(w_gu_q, w_gu_s, g_gu, h, r, c);
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < h; ++r)
+    for (int64_t c = 0; c < I; ++c) wd[r * I + c] = orc_nvfp4_value(w_d_q, w_d_s, g_d, I, r, c);
   for (int64_t r = 0; r < m; ++r) {
 #pragma omp parallel for schedule(static)
     for (int64_t c = 0; c < I; ++c) {
       double g = 0.0, u = 0.0;
       for (int64_t d = 0; d < h; ++d) {
         double xv = orc_bf16_to_double(x[r * h + d]);
-        g += xv * orc_nvfp4_value(w_gu_q, w_gu_s, g_gu, h, c, d);
-        u += xv * orc_nvfp4_value(w_gu_q, w_gu_s, g_gu, h, I + c, d);
+        g += xv * gu[c * h + d];
+        u += xv * gu[(I + c) * h + d];
       }
       a[c] = orc_bf16_to_double(orc_bf16_from_double(orc_silu(g) * u));
     }
 #pragma omp parallel for schedule(static)
     for (int64_t d = 0; d < h; ++d) {
       double o = 0.0;
-      for (int64_t c = 0; c < I; ++c) o += a[c] * orc_nvfp4_value(w_d_q, w_d_s, g_d, I, d, c);
+      for (int64_t c = 0; c < I; ++c) o += a[c] * wd[d * I + c];
       out[r * h + d] = o;
     }
   }
+  free(gu);
+  free(wd);
   free(a);
 }
 

@@ -45,10 +45,13 @@ int check_config(const moe_config* c) {
   if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k)
     return fail(MOE_ERR_INVALID, "the kept groups hold fewer than k experts");
   if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return fail(MOE_ERR_INVALID, "unknown score");
-  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_BLOCK128) return fail(MOE_ERR_INVALID, "unknown dtype");
+  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_BLOCK128 && c->dtype != MOE_DTYPE_NVFP4)
+    return fail(MOE_ERR_INVALID, "unknown dtype");
   if (c->E > 1024) return fail(MOE_ERR_UNSUPPORTED, "E > 1024");
   if (c->h % 256 != 0) return fail(MOE_ERR_UNSUPPORTED, "h must be a multiple of 256");
   if (c->I % 128 != 0) return fail(MOE_ERR_UNSUPPORTED, "I must be a multiple of 128");
+  if (c->dtype == MOE_DTYPE_NVFP4 && c->I % 256 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 weights need I to be a multiple of 256");
   if (c->I_shared != 0 && c->I_shared != c->I) return fail(MOE_ERR_UNSUPPORTED, "I_shared must be 0 or I");
   if ((int64_t)c->T * (c->k + 1) > INT32_MAX) return fail(MOE_ERR_UNSUPPORTED, "T * (k + 1) exceeds int32 rows");
   if (!(c->capacity_factor >= 0.f)) return fail(MOE_ERR_INVALID, "capacity_factor must be >= 0");
@@ -304,6 +307,53 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
     counted(2);
     return MOE_OK;
   }
+  if (c->dtype == MOE_DTYPE_NVFP4) {
+    moe::GroupedGemmFp4Desc g;
+    g.slot_expert = slot_expert;
+    g.n_experts = c->E;
+    g.A = xd;
+    g.a_rows = L.R_tot;
+    g.Bq = w->w_gu;
+    g.Bs = w->s_gu;
+    g.Bg = w->g_gu;
+    g.Bq_shared = shared ? w->w_gu_shared : nullptr;
+    g.Bs_shared = shared ? w->s_gu_shared : nullptr;
+    g.Bg_shared = shared ? w->g_gu_shared : nullptr;
+    g.b_rows = 2 * (int64_t)c->I;
+    g.offsets = offsets;
+    g.E = S;
+    g.R = (int)L.R;
+    g.T = c->T;
+    g.K = c->h;
+    g.N = 2 * c->I;
+    g.I = c->I;
+    g.mode = 0;
+    g.out = at<void>(ws, L.l.hbuf);
+    g.ldo = c->I;
+    g.row_weight = nullptr;
+    g.status = status_ptr(ws, L.l);
+    cudaError_t e = moe::launch_grouped_gemm_nvfp4(g, stream, &err);
+    if (e != cudaSuccess)
+      return err.empty() ? cuda_fail(e, "NVFP4 gate/up grouped GEMM launch") : cuda_fail(e, err.c_str());
+    g.A = at<void>(ws, L.l.hbuf);
+    g.Bq = w->w_d;
+    g.Bs = w->s_d;
+    g.Bg = w->g_d;
+    g.Bq_shared = shared ? w->w_d_shared : nullptr;
+    g.Bs_shared = shared ? w->s_d_shared : nullptr;
+    g.Bg_shared = shared ? w->g_d_shared : nullptr;
+    g.b_rows = c->h;
+    g.K = c->I;
+    g.N = c->h;
+    g.mode = 1;
+    g.out = yd;
+    g.ldo = c->h;
+    g.row_weight = row_weight;
+    e = moe::launch_grouped_gemm_nvfp4(g, stream, &err);
+    if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "NVFP4 down grouped GEMM launch") : cuda_fail(e, err.c_str());
+    counted(2);
+    return MOE_OK;
+  }
   auto launch = use_pair_tiles(c, S) ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
   moe::GroupedGemmDesc g;
   g.slot_expert = slot_expert;
@@ -351,13 +401,18 @@ int check_expert_weights(const moe_config* c, const moe_weights* w) {
     REQUIRE_PTR(w->w_gu_shared, "weights->w_gu_shared");
     REQUIRE_PTR(w->w_d_shared, "weights->w_d_shared");
   }
-  if (c->dtype == MOE_DTYPE_FP8_BLOCK128) {
+  if (c->dtype == MOE_DTYPE_FP8_BLOCK128 || c->dtype == MOE_DTYPE_NVFP4) {
     REQUIRE_PTR(w->s_gu, "weights->s_gu");
     REQUIRE_PTR(w->s_d, "weights->s_d");
     if (c->I_shared > 0) {
       REQUIRE_PTR(w->s_gu_shared, "weights->s_gu_shared");
       REQUIRE_PTR(w->s_d_shared, "weights->s_d_shared");
     }
+  }
+  if (c->dtype == MOE_DTYPE_NVFP4) {
+    if (!w->g_gu || !w->g_d) return fail(MOE_ERR_INVALID, "weights->g_gu / g_d is NULL");
+    if (c->I_shared > 0 && (!w->g_gu_shared || !w->g_d_shared))
+      return fail(MOE_ERR_INVALID, "weights->g_gu_shared / g_d_shared is NULL");
   }
   return MOE_OK;
 }
@@ -562,6 +617,20 @@ MOE_EXPORT int moe_quantize_weights_fp8(const void* w, int64_t batch, int64_t ro
   cudaError_t e = moe::launch_quantize_weights(w, batch, rows, cols, q, s, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "weight quantisation launch");
   if (batch * (rows / 128) * (cols / 128) > 0) counted(1);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_quantize_weights_nvfp4(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, void* s,
+                                          float* g, moe_stream_t stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return fail(MOE_ERR_INVALID, "negative size");
+  if (cols % 256) return fail(MOE_ERR_UNSUPPORTED, "cols must be a multiple of 256");
+  if (batch > 65535) return fail(MOE_ERR_UNSUPPORTED, "batch > 65535");
+  REQUIRE_PTR(w, "w");
+  REQUIRE_PTR(q, "q");
+  if (!s || !g) return fail(MOE_ERR_INVALID, "s or g is NULL");
+  cudaError_t e = moe::launch_quantize_weights_nvfp4(w, batch, rows, cols, q, s, g, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "NVFP4 weight quantisation launch");
+  if (batch * rows * cols > 0) counted(3);
   return MOE_OK;
 }
 

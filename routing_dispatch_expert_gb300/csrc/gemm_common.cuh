@@ -135,6 +135,8 @@ cudaError_t tma_encoder_ready();
 bool tma_encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t rows, int64_t K,
                    int box_rows);
 // [G, rows, K] row-major stack; box = 1 x box_rows x 128 bytes of K, 128-byte swizzle.
+// [G, rows, K] bytes, no swizzle, box = box_k bytes x box_rows rows (box_k * elem a multiple of 16).
+bool tma_encode_3d_plain(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_t K, int box_k, int box_rows);
 bool tma_encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t G, int64_t rows,
                    int64_t K, int box_rows);
 

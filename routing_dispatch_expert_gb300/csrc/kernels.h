@@ -110,6 +110,35 @@ struct GroupedGemmFp8Desc {
 };
 cudaError_t launch_grouped_gemm_fp8(const GroupedGemmFp8Desc& d, cudaStream_t stream, std::string* err);
 
+// Step 3, NVFP4-weight layer: bf16 activations, expert weights as e2m1 codes [E, N, K/2], e4m3 block
+// scales [E, N, K/16] (one per 16 elements along K) and fp32 matrix scales [E]; expanded to bf16 in
+// shared memory and multiplied on the bf16 tensor cores. Modes 0 and 1 as the bf16 kernel.
+struct GroupedGemmFp4Desc {
+  const void* A;  // [a_rows, K] bf16
+  int64_t a_rows;
+  const void* Bq;        // [E, b_rows, K/2] codes
+  const void* Bs;        // [E, b_rows, K/16] e4m3 block scales
+  const float* Bg;       // [E] matrix scales
+  const void* Bq_shared; // [b_rows, K/2] shared expert or nullptr
+  const void* Bs_shared;
+  const float* Bg_shared;
+  int64_t b_rows;
+  const int32_t* offsets;
+  const int32_t* slot_expert = nullptr;
+  int n_experts = 0;
+  int E, R, T, K, N, I;
+  int mode;
+  void* out;
+  int ldo;
+  const float* row_weight;
+  int* status;
+};
+cudaError_t launch_grouped_gemm_nvfp4(const GroupedGemmFp4Desc& d, cudaStream_t stream, std::string* err);
+// NVFP4 quantisation of `batch` bf16 matrices [rows, cols] (cols % 256 == 0): the matrix amax is
+// gathered in g itself, the blocks are quantised, then g is turned into the matrix scales.
+cudaError_t launch_quantize_weights_nvfp4(const void* w, int64_t batch, int64_t rows, int64_t cols, void* q, void* s,
+                                          float* g, cudaStream_t stream);
+
 // Step 4: combine.
 cudaError_t launch_combine(const void* yd, const int32_t* inv_pos, void* y, int T, int h, int k, int shared,
                            cudaStream_t stream);

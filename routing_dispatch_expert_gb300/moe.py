@@ -17,7 +17,8 @@ SO_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = 0, -1, -2, -3, -4, -5
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
-MOE_DTYPE_BF16, MOE_DTYPE_FP8_BLOCK128 = 0, 1
+DTYPES = {"bf16": 0, "fp8": 1, "nvfp4": 2}
+MOE_DTYPE_BF16, MOE_DTYPE_FP8_BLOCK128, MOE_DTYPE_NVFP4 = 0, 1, 2
 MOE_LOGITS_GIVEN = 1
 MOE_STATUS_BAD_EXPERT_INDEX, MOE_STATUS_WAIT_TIMEOUT = 1, 2
 
@@ -43,7 +44,8 @@ class MoeConfig(ctypes.Structure):
 
 class MoeWeightsStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w_router", "bias", "w_gu", "s_gu", "w_d", "s_d", "w_gu_shared",
-                                               "s_gu_shared", "w_d_shared", "s_d_shared")]
+                                               "s_gu_shared", "w_d_shared", "s_d_shared", "g_gu", "g_d",
+                                               "g_gu_shared", "g_d_shared")]
 
 
 class MoeWsLayout(ctypes.Structure):
@@ -77,6 +79,7 @@ def load():
                 "moe_combine": [cfgp, vp, vp, vp, vp],
                 "moe_forward": [cfgp, vp, wp, vp, vp, sz, vp],
                 "moe_quantize_weights_fp8": [vp, i64, i64, i64, vp, vp, vp],
+                "moe_quantize_weights_nvfp4": [vp, i64, i64, i64, vp, vp, vp, vp],
                 "moe_device_status": [cfgp, vp, ctypes.POINTER(ctypes.c_int32), vp],
                 "moe_graph_create": [cfgp, vp, wp, vp, vp, sz, vp, ctypes.POINTER(vp)],
                 "moe_graph_launch": [vp, vp],
@@ -112,7 +115,7 @@ def make_config(T, h, E, k, I, I_shared=0, n_group=1, topk_group=1, score="softm
                 dtype="bf16", capacity_factor=0.0, placement: "Placement | None" = None) -> MoeConfig:
     cfg = MoeConfig(T, h, E, k, I, I_shared, n_group, topk_group,
                     MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID, int(bool(renorm)),
-                    float(routed_scale), MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP8_BLOCK128,
+                    float(routed_scale), DTYPES[dtype],
                     float(capacity_factor), None if placement is None else ctypes.pointer(placement.struct))
     cfg._placement = placement  # keep the tables alive as long as the config
     return cfg
@@ -152,13 +155,16 @@ class Placement:
 
 class Weights:
     """Device tensors of one layer and their C struct. bf16 expert weights for dtype 'bf16'; for
-    'fp8' pass e4m3 codes (torch.uint8) and fp32 128x128 scales (see quantize_weights_fp8)."""
+    'fp8' pass e4m3 codes (torch.uint8) and fp32 128x128 scales (see quantize_weights_fp8); for
+    'nvfp4' pass codes, e4m3 block scales and fp32 matrix scales (see quantize_weights_nvfp4)."""
 
     def __init__(self, w_router, bias=None, w_gu=None, w_d=None, w_gu_shared=None, w_d_shared=None, s_gu=None,
-                 s_d=None, s_gu_shared=None, s_d_shared=None):
+                 s_d=None, s_gu_shared=None, s_d_shared=None, g_gu=None, g_d=None, g_gu_shared=None,
+                 g_d_shared=None):
         self.tensors = dict(w_router=w_router, bias=bias, w_gu=w_gu, s_gu=s_gu, w_d=w_d, s_d=s_d,
                             w_gu_shared=w_gu_shared, s_gu_shared=s_gu_shared, w_d_shared=w_d_shared,
-                            s_d_shared=s_d_shared)
+                            s_d_shared=s_d_shared, g_gu=g_gu, g_d=g_d, g_gu_shared=g_gu_shared,
+                            g_d_shared=g_d_shared)
         self.struct = MoeWeightsStruct(**{n: (None if t is None else t.data_ptr()) for n, t in self.tensors.items()})
 
 
@@ -230,6 +236,19 @@ def quantize_weights_fp8(w: torch.Tensor):
     s = torch.empty(tuple(w.shape[:-2]) + (rows // 128, cols // 128), dtype=torch.float32, device=w.device)
     _check(load().moe_quantize_weights_fp8(_ptr(w), batch, rows, cols, _ptr(q), _ptr(s), _stream()))
     return q, s
+
+
+def quantize_weights_nvfp4(w: torch.Tensor):
+    """NVFP4 quantisation of bf16 weights [..., rows, cols] -> (codes uint8 [..., rows, cols/2], e4m3 block
+    scales uint8 [..., rows, cols/16], fp32 matrix scales [...])."""
+    rows, cols = w.shape[-2], w.shape[-1]
+    batch = w.numel() // (rows * cols)
+    lead = tuple(w.shape[:-2])
+    q = torch.empty(lead + (rows, cols // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty(lead + (rows, cols // 16), dtype=torch.uint8, device=w.device)
+    g = torch.empty(lead if lead else (1,), dtype=torch.float32, device=w.device)
+    _check(load().moe_quantize_weights_nvfp4(_ptr(w), batch, rows, cols, _ptr(q), _ptr(s), _ptr(g), _stream()))
+    return q, s, g
 
 
 def launch_count() -> int:

@@ -44,7 +44,7 @@ class Workload:
     score: str  # "softmax" | "sigmoid"
     renorm: bool
     routed_scale: float
-    dtype: str  # "bf16" | "fp8"
+    dtype: str  # "bf16" | "fp8" | "nvfp4" (the expert weights' storage type; generated as bf16)
     seed: int
     bias_range: float | None = None  # bias ~ U(-b, b)
     zipf_s: float | None = None  # popularity skew of the router logits
@@ -77,6 +77,8 @@ WORKLOADS: dict[str, Workload] = {
     "dsv3_prefill": Workload("dsv3_prefill", T=16384, dtype="bf16", seed=2, **_DSV3),
     "dsv3_decode": Workload("dsv3_decode", T=256, dtype="bf16", seed=3, zipf_s=1.2, **_DSV3),
     "dsv3_fp8": Workload("dsv3_fp8", T=32768, dtype="fp8", seed=4, zipf_s=1.0, **_DSV3),
+    # the decode layer with NVFP4 expert weights (FP4 MoE weights of the Blackwell deployment)
+    "dsv3_decode_fp4": Workload("dsv3_decode_fp4", T=256, dtype="nvfp4", seed=3, zipf_s=1.2, **_DSV3),
 }
 
 

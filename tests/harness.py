@@ -23,6 +23,11 @@ def cfg_of(wl: synth.Workload) -> rde.MoeConfig:
                            dtype=wl.dtype, capacity_factor=wl.capacity_factor)
 
 
+def config_capacity_factor(wl: synth.Workload) -> float:
+    """The capacity factor as the layer config holds it (fp32): the oracle must see the same number."""
+    return float(np.float32(wl.capacity_factor))
+
+
 def route_kwargs(wl: synth.Workload) -> dict:
     return dict(k=wl.k, n_group=wl.n_group, topk_group=wl.topk_group,
                 score=oracle.SOFTMAX if wl.score == "softmax" else oracle.SIGMOID, renorm=wl.renorm,
@@ -65,6 +70,9 @@ class GpuLayer:
             if wl.has_shared:
                 ws["w_gu_shared"], ws["s_gu_shared"] = rde.quantize_weights_fp8(self.inp["w_gu_shared"])
                 ws["w_d_shared"], ws["s_d_shared"] = rde.quantize_weights_fp8(self.inp["w_d_shared"])
+        elif wl.dtype == "nvfp4":
+            for n in ("gu", "d") + (("gu_shared", "d_shared") if wl.has_shared else ()):
+                ws["w_" + n], ws["s_" + n], ws["g_" + n] = rde.quantize_weights_nvfp4(self.inp["w_" + n])
         else:
             for n in ("w_gu", "w_d", "w_gu_shared", "w_d_shared"):
                 ws[n] = self.inp[n]
@@ -126,6 +134,8 @@ def oracle_tokens(layer: GpuLayer, tokens: np.ndarray, idx: np.ndarray, w: np.nd
         if fp8:
             (gq, gs), (dq, ds) = oracle.quant_weight_128x128(gu), oracle.quant_weight_128x128(d)
             return oracle.expert_ffn_fp8(xq[rows], xsc[rows], gq, gs, dq, ds)
+        if wl.dtype == "nvfp4":
+            return oracle.expert_ffn_nvfp4(xs[rows], oracle.quant_weight_nvfp4(gu), oracle.quant_weight_nvfp4(d))
         return oracle.expert_ffn_bf16(xs[rows], gu, d)
 
     sel = idx[tokens]

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_sizes_match_header_layout():
     assert ctypes.sizeof(moe.MoeConfig) == 13 * 4 + 4 + 8  # 13 scalars, padding, placement pointer
     assert ctypes.sizeof(moe.MoePlacement) == 2 * 4 + 4 * 8
-    assert ctypes.sizeof(moe.MoeWeightsStruct) == 10 * 8
+    assert ctypes.sizeof(moe.MoeWeightsStruct) == 14 * 8
     assert ctypes.sizeof(moe.MoeWsLayout) == 16 * 8
 
 
@@ -62,6 +62,7 @@ def _cfg(**kw):
     (dict(I_shared=256), moe.MOE_ERR_UNSUPPORTED),
     (dict(E=2048, k=2), moe.MOE_ERR_UNSUPPORTED),
     (dict(T=-1), moe.MOE_ERR_INVALID),
+    (dict(dtype="nvfp4", I=128), moe.MOE_ERR_UNSUPPORTED),  # NVFP4 block scales need I % 256 == 0
 ])
 def test_config_validation(lib, kw, code):
     n = ctypes.c_size_t()
@@ -96,6 +97,9 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert rc == moe.MOE_ERR_WORKSPACE
     rc = lib.moe_quantize_weights_fp8(ctypes.c_void_p(0x1000), 1, 100, 128, ctypes.c_void_p(0x1000),
                                       ctypes.c_void_p(0x1000), None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    rc = lib.moe_quantize_weights_nvfp4(ctypes.c_void_p(0x1000), 1, 64, 128, ctypes.c_void_p(0x1000),
+                                        ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
 
 

@@ -34,7 +34,8 @@ def _sample(n, count, seed):
     return np.array(sorted(s))
 
 
-@pytest.mark.parametrize("name,n_tok", [("mixtral", 4), ("dsv3_prefill", 8), ("dsv3_decode", 16), ("dsv3_fp8", 8)])
+@pytest.mark.parametrize("name,n_tok", [("mixtral", 4), ("dsv3_prefill", 8), ("dsv3_decode", 16), ("dsv3_fp8", 8),
+                                        ("dsv3_decode_fp4", 8)])
 def test_full_size_layer(name, n_tok):
     wl = synth.WORKLOADS[name]
     L = GpuLayer(wl)

@@ -8,8 +8,8 @@ import oracle
 import synth
 import routing_dispatch_expert_gb300 as rde
 from routing_dispatch_expert_gb300 import build as pkg_build
-from harness import (BF16_TOL, FP8_TOL, MARGIN, WEIGHT_RTOL, GpuLayer, bits, cfg_of, logit_tolerance,
-                     oracle_tokens, rel_err_per_token, route_kwargs, selection_margin)
+from harness import (BF16_TOL, FP8_TOL, MARGIN, WEIGHT_RTOL, GpuLayer, bits, cfg_of, config_capacity_factor,
+                     logit_tolerance, oracle_tokens, rel_err_per_token, route_kwargs, selection_margin)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,12 @@ SMALL = {
                                           capacity_factor=1.25),
     "cap_mixtral": _W["mixtral"].replace(name="cap_mixtral", T=500, h=512, I=256, capacity_factor=1.0),
     "cap_fp8": _W["dsv3_fp8"].replace(name="cap_fp8", T=200, h=256, E=32, I=128, I_shared=128, capacity_factor=1.1),
+    # NVFP4 expert weights (e2m1 codes, e4m3 scales per 16, fp32 per matrix), bf16 activations
+    "fp4_small": _W["dsv3_decode_fp4"].replace(name="fp4_small", T=300, h=512, E=64, I=256, I_shared=256),
+    "fp4_mixtral": _W["mixtral"].replace(name="fp4_mixtral", T=333, h=512, I=512, dtype="nvfp4"),
+    "fp4_e256": _W["dsv3_decode_fp4"].replace(name="fp4_e256", T=130, h=256, E=256, I=256, I_shared=256),
+    "cap_fp4": _W["dsv3_decode_fp4"].replace(name="cap_fp4", T=200, h=256, E=32, I=256, I_shared=0,
+                                             capacity_factor=1.2),
     # at least 1024 rows per expert on average: the bf16 expert GEMMs run on CTA pairs (256-row tiles)
     "pair_mixtral": _W["mixtral"].replace(name="pair_mixtral", T=4500, h=512, I=384),
     "pair_dsv3": _W["dsv3_prefill"].replace(name="pair_dsv3", T=2600, h=512, E=8, k=4, n_group=2, topk_group=1,
@@ -77,7 +83,8 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
 
     # the whole layer on identical logits
     ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, fp8=wl.dtype == "fp8",
-                         capacity_factor=wl.capacity_factor, **route_kwargs(wl))
+                         nvfp4=wl.dtype == "nvfp4", capacity_factor=config_capacity_factor(wl),
+                         **route_kwargs(wl))
     np.testing.assert_array_equal(it["topk_idx"].cpu().numpy(), ref["topk_idx"])
     np.testing.assert_allclose(it["topk_w"].cpu().numpy(), ref["topk_w"], rtol=WEIGHT_RTOL, atol=1e-7)
     np.testing.assert_array_equal(it["counts"].cpu().numpy(), ref["counts"])
@@ -282,6 +289,24 @@ def test_fp8_dispatch_is_bit_exact():
     np.testing.assert_array_equal(xs[T * k:].cpu().numpy(), xsc)
 
 
+def test_nvfp4_weight_quantiser_is_bit_exact():
+    g = torch.Generator(device="cpu").manual_seed(4)
+    w = torch.randn(3, 64, 512, generator=g) * 0.02 * torch.exp(torch.randn(3, 64, 1, generator=g))
+    w[1] = 0.0  # an all-zero matrix -> matrix scale 1, all codes and scales zero
+    w[2, :, :16] = 0.0  # a zero block inside a nonzero matrix
+    w[2, 3, 100] = 7.0  # an outlier: every other block of the matrix gets a small e4m3 scale
+    wb = w.to(torch.bfloat16).cuda()
+    q, sc, gs = rde.quantize_weights_nvfp4(wb)
+    torch.cuda.synchronize()
+    wbits = bits(wb)
+    for b in range(3):
+        rq, rs, rg = oracle.quant_weight_nvfp4(wbits[b])
+        np.testing.assert_array_equal(q[b].cpu().numpy(), rq)
+        np.testing.assert_array_equal(sc[b].cpu().numpy(), rs)
+        assert gs[b].item() == rg
+    assert gs[1].item() == 1.0
+
+
 def test_fp8_weight_quantiser_is_bit_exact():
     g = torch.Generator(device="cpu").manual_seed(3)
     w = (torch.randn(3, 256, 384, generator=g) * 0.02)
@@ -338,7 +363,7 @@ def test_routing_near_ties_bit_exact(score):
 
 
 @pytest.mark.parametrize("dtype,cf,pairs", [("bf16", 0.0, False), ("fp8", 0.0, False), ("bf16", 1.1, False),
-                                            ("bf16", 0.0, True), ("fp8", 0.0, True)])
+                                            ("nvfp4", 0.0, False), ("bf16", 0.0, True), ("fp8", 0.0, True)])
 def test_eplb_placement_matches_unplaced_layer(dtype, cf, pairs):
     """An EPLB placement (redundant replicas, card-major slots) only reorders the expert-major rows:
     the per-slot permutation matches the oracle and the layer output is bit-identical. With `pairs`
@@ -371,7 +396,7 @@ def test_eplb_placement_matches_unplaced_layer(dtype, cf, pairs):
     counts = rde.ws_view(ws, cfg, "counts", torch.int32, (S,)).cpu().numpy()
     offsets = rde.ws_view(ws, cfg, "offsets", torch.int32, (S + 1,)).cpu().numpy()
     inv_pos = rde.ws_view(ws, cfg, "inv_pos", torch.int32, (base.T, base.k)).cpu().numpy()
-    cap = oracle.capacity(cf, base.T, base.k, base.E)
+    cap = oracle.capacity(config_capacity_factor(base), base.T, base.k, base.E)
     rc, ro, ri, rt = oracle.permute_placed(idx, base.E, plan["slot_expert"], plan["slot_replica"], plan["replicas"],
                                            cap)
     np.testing.assert_array_equal(counts, rc)
@@ -393,7 +418,7 @@ def test_balance_stats_match_the_oracle_counts(cf):
     L.forward()
     idx = L.intermediates()["topk_idx"].cpu().numpy()
     b = rde.balance(L.cfg, L.ws)
-    cap = oracle.capacity(cf, wl.T, wl.k, wl.E)
+    cap = oracle.capacity(config_capacity_factor(wl), wl.T, wl.k, wl.E)
     counts, offsets, _, _ = oracle.permute_capacity(idx, wl.E, cap)
     assert b["counts"] == counts.tolist()
     assert b["dropped"] == wl.T * wl.k - int(offsets[-1])
