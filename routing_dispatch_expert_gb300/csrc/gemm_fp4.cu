@@ -86,17 +86,27 @@ struct BlockTable {
   uint32_t lo_a, lo_b, hi_a, hi_b;
 };
 
+// e4m3 code of a (non-negative) block scale -> bf16 bits, exact: normal codes move the 4-bit exponent
+// to the bf16 bias and the 3 mantissa bits up; subnormal codes (m x 2^-9) take the float route.
+__device__ __forceinline__ uint32_t e4m3_bf16_bits(uint32_t code) {
+  const uint32_t e = (code >> 3) & 0xF, m = code & 7;
+  if (e != 0) return ((e + 120) << 7) | (m << 4);
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)m * 0.001953125f));
+}
+
 __device__ __forceinline__ BlockTable block_table(uint32_t scale_code) {
-  const __half_raw sr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)scale_code, __NV_E4M3);
-  const float sc = __half2float(*reinterpret_cast<const __half*>(&sr));
-  // e2m1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (OCP Microscaling formats)
-  const __nv_bfloat162 t01 = __float22bfloat162_rn(make_float2(0.0f, 0.5f * sc));
-  const __nv_bfloat162 t23 = __float22bfloat162_rn(make_float2(sc, 1.5f * sc));
-  const __nv_bfloat162 t45 = __float22bfloat162_rn(make_float2(2.0f * sc, 3.0f * sc));
-  const __nv_bfloat162 t67 = __float22bfloat162_rn(make_float2(4.0f * sc, 6.0f * sc));
-  const uint32_t a = *reinterpret_cast<const uint32_t*>(&t01), b = *reinterpret_cast<const uint32_t*>(&t23);
-  const uint32_t c = *reinterpret_cast<const uint32_t*>(&t45), d = *reinterpret_cast<const uint32_t*>(&t67);
-  return {prmt(a, b, 0x6420), prmt(c, d, 0x6420), prmt(a, b, 0x7531), prmt(c, d, 0x7531)};
+  const uint32_t sb = e4m3_bf16_bits(scale_code);
+  const uint32_t s2u = sb | (sb << 16);
+  const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
+  // the e2m1 magnitudes 0, 0.5 | 1, 1.5 | 2, 3 | 4, 6 (OCP Microscaling formats) as bf16 pairs
+  const uint32_t k[4] = {0x3F000000u, 0x3FC03F80u, 0x40404000u, 0x40C04080u};
+  uint32_t t[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // products with at most 6 significant bits: exact in bf16
+    const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&k[i]), s2);
+    t[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return {prmt(t[0], t[1], 0x6420), prmt(t[2], t[3], 0x6420), prmt(t[0], t[1], 0x7531), prmt(t[2], t[3], 0x7531)};
 }
 
 // Four e2m1 codes (the low 16 bits of g, element i in nibble i) -> four bf16 in two words. The
