@@ -41,6 +41,10 @@ SMALL = {
     "fp4_e256": _W["dsv3_decode_fp4"].replace(name="fp4_e256", T=130, h=256, E=256, I=256, I_shared=256),
     "cap_fp4": _W["dsv3_decode_fp4"].replace(name="cap_fp4", T=200, h=256, E=32, I=256, I_shared=0,
                                              capacity_factor=1.2),
+    # large expert groups (several 128-row tiles per expert)
+    "fp4_large_groups": _W["dsv3_decode_fp4"].replace(name="fp4_large_groups", T=2200, h=512, E=8, k=4,
+                                                      n_group=2, topk_group=1, I=256, I_shared=256),
+    "fp4_mixtral_large": _W["mixtral"].replace(name="fp4_mixtral_large", T=1100, h=256, I=256, dtype="nvfp4"),
     # at least 1024 rows per expert on average: the bf16 expert GEMMs run on CTA pairs (256-row tiles)
     "pair_mixtral": _W["mixtral"].replace(name="pair_mixtral", T=4500, h=512, I=384),
     "pair_dsv3": _W["dsv3_prefill"].replace(name="pair_dsv3", T=2600, h=512, E=8, k=4, n_group=2, topk_group=1,
