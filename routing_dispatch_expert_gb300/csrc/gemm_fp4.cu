@@ -11,10 +11,8 @@
 // The weight tile travels in FP4 (9 KB of codes and scales per 256 x 64 tile instead of 32 KB of
 // bf16) and is expanded in shared memory: e2m1 x e4m3 has at most 6 significant bits, so the product
 // is exact in bf16, and the bf16 tensor-core MMA then runs unchanged; the fp32 matrix scale
-// multiplies the accumulator in the epilogue. The expansion is byte permutes (prmt) from a per-block
-// table of the eight products, built once per 16 elements: per-element float conversions ran at a
-// fraction of the integer rate and held a decode step at a quarter of the HBM bandwidth. (The
-// block-scaled FP4 MMA would need FP4 activations as well.)
+// multiplies the accumulator in the epilogue. (The block-scaled FP4 MMA would need FP4 activations as
+// well.)
 //
 // Roles, 448 threads: warp 0 lane 0 TMA producer (activation tile, weight codes and scales), warp 1
 // lane 0 MMA issuer, warps 2-5 epilogue, warps 6-13 expand the weight tile (one row per thread: 32
@@ -74,51 +72,14 @@ using grp::silu;
 using grp::Tile;
 using grp::wait_or_abort;
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// The 8 magnitudes of one 16-element block (e2m1 value x e4m3 scale, exact in bf16) as byte tables
-// for prmt: lo = low bytes of entries 0-3 / 4-7, hi = high bytes.
-struct BlockTable {
-  uint32_t lo_a, lo_b, hi_a, hi_b;
-};
-
-// e4m3 code of a (non-negative) block scale -> bf16 bits, exact: normal codes move the 4-bit exponent
-// to the bf16 bias and the 3 mantissa bits up; subnormal codes (m x 2^-9) take the float route.
-__device__ __forceinline__ uint32_t e4m3_bf16_bits(uint32_t code) {
-  const uint32_t e = (code >> 3) & 0xF, m = code & 7;
-  if (e != 0) return ((e + 120) << 7) | (m << 4);
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)m * 0.001953125f));
-}
-
-__device__ __forceinline__ BlockTable block_table(uint32_t scale_code) {
-  const uint32_t sb = e4m3_bf16_bits(scale_code);
-  const uint32_t s2u = sb | (sb << 16);
-  const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
-  // the e2m1 magnitudes 0, 0.5 | 1, 1.5 | 2, 3 | 4, 6 (OCP Microscaling formats) as bf16 pairs
-  const uint32_t k[4] = {0x3F000000u, 0x3FC03F80u, 0x40404000u, 0x40C04080u};
-  uint32_t t[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {  // products with at most 6 significant bits: exact in bf16
-    const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&k[i]), s2);
-    t[i] = *reinterpret_cast<const uint32_t*>(&v);
-  }
-  return {prmt(t[0], t[1], 0x6420), prmt(t[2], t[3], 0x6420), prmt(t[0], t[1], 0x7531), prmt(t[2], t[3], 0x7531)};
-}
-
-// Four e2m1 codes (the low 16 bits of g, element i in nibble i) -> four bf16 in two words. The
-// magnitude (low 3 bits of a nibble) selects a table byte; the sign bit (bit 3) in prmt's
-// sign-replicating mode turns a 0x80 source byte into 0xff, which becomes the 0x80 sign byte.
-__device__ __forceinline__ uint2 expand4(uint32_t g, const BlockTable& t) {
-  const uint32_t sel = g & 0x7777u;
-  const uint32_t lo = prmt(t.lo_a, t.lo_b, sel);
-  uint32_t hi = prmt(t.hi_a, t.hi_b, sel);
-  const uint32_t neg = prmt(0x80808080u, 0x80808080u, g & 0xFFFFu) ^ 0x80808080u;  // 0x7f where negative
-  hi ^= (neg + 0x01010101u) & 0x80808080u;
-  return make_uint2(prmt(lo, hi, 0x5140), prmt(lo, hi, 0x7362));
+// e2m1 pair (low nibble -> low half) times an e4m3 scale, as two exact bf16 values: the hardware
+// converts the pair to f16x2, the product with the scale (at most 6 significant bits) is exact in f16
+// and in bf16.
+__device__ __forceinline__ uint32_t expand2(uint32_t byte, __half2 s2) {
+  const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)byte, __NV_E2M1);
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&r), s2);
+  const __nv_bfloat162 b = __float22bfloat162_rn(__half22float2(v));
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -282,14 +243,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         uint8_t* brow = ring_b + bst * B_BYTES + n * 128;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {  // 16-element scale blocks
-          const BlockTable tb = block_table((sc4 >> (8 * b)) & 0xFF);
+        for (int b = 0; b < 4; ++b) {
+          const __half_raw sr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sc4 >> (8 * b)) & 0xFF), __NV_E4M3);
+          const __half sh = *reinterpret_cast<const __half*>(&sr);
+          const __half2 s2 = __halves2half2(sh, sh);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {  // 8-element chunks = 16-byte units of the swizzled row
+          for (int h = 0; h < 2; ++h) {
             const int c = 2 * b + h;
             const uint32_t w = words[c];
-            const uint2 e0 = expand4(w, tb), e1 = expand4(w >> 16, tb);
-            *reinterpret_cast<uint4*>(brow + ((c ^ (n & 7)) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+            const uint4 o = make_uint4(expand2(w & 0xFF, s2), expand2((w >> 8) & 0xFF, s2),
+                                       expand2((w >> 16) & 0xFF, s2), expand2(w >> 24, s2));
+            *reinterpret_cast<uint4*>(brow + ((c ^ (n & 7)) << 4)) = o;
           }
         }
         fence_proxy_async_smem();  // the tensor core reads this tile through the async proxy
