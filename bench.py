@@ -67,7 +67,7 @@ def layer_counts(wl, active_experts):
     return flops, gemm_flops, bytes_
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_fp8.cu", "gemm_common.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_fp8.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh")
 
 
 def gemm_source_sha():
