@@ -456,7 +456,7 @@ def main():
         gemm_kernel = "grouped_gemm_fp8_kernel"
     elif wl.dtype == "nvfp4":
         gemm_kernel = "grouped_gemm_nvfp4_kernel"
-    elif wl.T * wl.k >= 1024 * wl.E:
+    elif wl.T * wl.k >= 128 * wl.E:
         gemm_kernel = "grouped_gemm_bf16_pair_kernel"
     else:
         gemm_kernel = "grouped_gemm_bf16_kernel"

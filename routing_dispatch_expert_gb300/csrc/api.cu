@@ -244,11 +244,12 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   return MOE_OK;
 }
 
-// bf16 expert GEMMs: CTA-pair tiles (256 rows) keep the tensor pipe busier than single-CTA tiles (128
-// rows) but pad each expert's last tile to 256 rows: they pay off once the experts average at least
-// this many rows. (The FP8 kernel stays on single CTAs: its per-K-block promotion hand-off would have
-// to cross the pair every 128 K elements.)
-constexpr int64_t kPairMinRowsPerGroup = 1024;
+// bf16 expert GEMMs: CTA-pair tiles (256 rows, an expert's tail of at most 128 rows as a 128-row pair
+// tile) move less shared memory per MMA than single-CTA tiles, but each CTA stages only half a weight
+// tile per K step: a weight-streaming step (a few rows per expert) keeps more weight bytes in flight on
+// single CTAs. (The FP8 kernel stays on single CTAs: its per-K-block promotion hand-off would have to
+// cross the pair every 128 K elements.)
+constexpr int64_t kPairMinRowsPerGroup = 128;
 bool use_pair_tiles(const moe_config* c, int S) {
   return S > 0 && (int64_t)c->T * c->k >= kPairMinRowsPerGroup * S;
 }

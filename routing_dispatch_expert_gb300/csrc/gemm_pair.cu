@@ -13,8 +13,13 @@
 // in flight: 6 stages x 48 KB do not fit in 227 KB of shared memory. A CTA pair computes a 256 x 256
 // tile with one MMA stream: each CTA stages its own 128 rows of A and its own 128 columns of B, 32 KB
 // per step, so 6 stages (192 KB) cover the latency, and the weight tile is read from L2 once per 256
-// rows instead of once per 128. The cost is coarser row tiles (an expert's last tile is padded to 256
-// rows instead of 128).
+// rows instead of once per 128. An expert's last tile, when it holds at most 128 rows, is a half tile:
+// an M = 128 pair MMA (64 rows from each CTA), which runs at the same rate per SM, so the row padding
+// stays at the 128-row granularity of single-CTA tiles. Its accumulator lands differently: in each CTA,
+// lanes 0-63 hold the CTA's 64 rows for output columns [0, 128) and lanes 64-127 the same rows for
+// columns [128, 256), in 128 TMEM columns. For the gate/up launch the B rows of a half tile are
+// interleaved (leader: gate 0-63 and up 0-63 of the column tile; follower: gate 64-127 and up
+// 64-127), so each lane still holds the gate and up value of its outputs.
 //
 // Roles (192 threads per CTA; CTA rank 0 of the cluster is the leader):
 //   * warp 0 lane 0 of each CTA: TMA producer into its own 6-stage ring; completions are counted on
@@ -79,7 +84,8 @@ using grp::wait_or_abort;
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                                  const __grid_constant__ CUtensorMap tmBs, const Args args) {
+                                  const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB64,
+                                  const __grid_constant__ CUtensorMap tmBs64, const Args args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared s;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -106,6 +112,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       tma_prefetch_desc(&tmBs);
+      tma_prefetch_desc(&tmB64);
+      tma_prefetch_desc(&tmBs64);
     }
   }
   if (warp == 1) {
@@ -129,11 +137,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, PM);
-      const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
+      const bool half = t.rows <= BM;  // the M = 128 pair tile: 64 rows per CTA
+      const bool gu_half = half && args.mode == 0;
+      const CUtensorMap* mb = t.g < args.E ? (gu_half ? &tmB64 : &tmB) : (gu_half ? &tmBs64 : &tmBs);
       const int z = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) : 0;
-      const int a_row = t.a_row + (int)rank * BM;
-      // mode 0: the leader stages the 128 gate rows, the follower the matching up rows
-      const int n0 = args.mode == 0 ? (int)rank * args.I + t.n_tile * BNH : t.n_tile * BN + (int)rank * BNH;
+      const int a_row = t.a_row + (int)rank * (half ? BM / 2 : BM);
+      // mode 0: the leader stages the 128 gate rows, the follower the matching up rows (half tiles:
+      // each CTA stages 64 gate rows and the 64 matching up rows)
+      const int n0 = gu_half ? t.n_tile * BNH + (int)rank * (BNH / 2)
+                     : args.mode == 0 ? (int)rank * args.I + t.n_tile * BNH : t.n_tile * BN + (int)rank * BNH;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!wait_or_abort(&s.empty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
@@ -144,7 +156,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
         if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2 * STAGE_BYTES);
         tma_load_2d_pair(a, &tmA, fb, kb * BK, a_row);
-        tma_load_3d_pair(b, mb, fb, kb * BK, n0, z);
+        if (gu_half) {
+          tma_load_3d_pair(b, mb, fb, kb * BK, n0, z);
+          tma_load_3d_pair(b + B_BYTES / 2, mb, fb, kb * BK, args.I + n0, z);
+        } else {
+          tma_load_3d_pair(b, mb, fb, kb * BK, n0, z);
+        }
         ++issued;
         if (++stage == STAGES) {
           stage = 0;
@@ -161,13 +178,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer (leader)
-    const uint32_t idesc = idesc_bf16(PM, BN);
+    const uint32_t idesc_full = idesc_bf16(PM, BN), idesc_half = idesc_bf16(PM / 2, BN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
+      const uint32_t idesc = grp::decode(s.tb, G, args.n_tiles, tile, PM).rows <= BM ? idesc_half : idesc_full;
       if (!wait_or_abort(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) break;
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -210,17 +228,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      const int lr = (int)rank * BM + r;  // row within the pair tile
+      const bool half = t.rows <= BM;
+      // full tile: lane r of this CTA = row 128 rank + r, all 256 columns. Half tile: lanes 0-63 and
+      // 64-127 both hold rows 64 rank + (r mod 64), for output columns [0, 128) and [128, 256)
+      const int lr = half ? (int)rank * (BM / 2) + (r & 63) : (int)rank * BM + r;  // row within the pair tile
+      const int ch = half ? r >> 6 : 0;  // half tiles: which 128 output columns this lane holds
       const bool valid = lr < t.rows;
       const int64_t orow = (int64_t)t.a_row + lr;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (args.mode == 0) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * BNH;
+        // full: gate columns [0, 128), up [128, 256) -> H columns [0, 128) of the tile; half: gate
+        // columns [0, 64), up [64, 128) -> H columns [64 ch, 64 ch + 64)
+        const int ncol = half ? BNH / 2 : BNH;
+        const int up = half ? BNH / 2 : BNH;
+        __nv_bfloat16* out =
+            reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * BNH + ch * (BNH / 2);
 #pragma unroll 1
-        for (int c = 0; c < BNH; c += 32) {
+        for (int c = 0; c < ncol; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + BNH + c, u);
+          tmem_ld32(taddr + up + c, u);
           tmem_ld_wait_regs(g);
           tmem_ld_wait_regs(u);
           uint32_t p[16];
@@ -238,9 +265,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         const float w = (valid && t.g < args.E) ? args.row_weight[orow] : 1.0f;
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * BN;
+        const int ncol = half ? BN / 2 : BN;
+        __nv_bfloat16* out =
+            reinterpret_cast<__nv_bfloat16*>(args.out) + orow * args.ldo + t.n_tile * BN + ch * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < ncol; c += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + c, v);
           tmem_ld_wait_regs(v);
@@ -312,11 +341,14 @@ cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t
     }
     max_pairs = n < num_sms() / 2 ? n : num_sms() / 2;
   }
-  CUtensorMap tA, tB, tBs;
+  CUtensorMap tA, tB, tBs, tB64, tBs64;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int64_t G = d.n_experts > 0 ? d.n_experts : d.E;
   bool ok = tma_encode_2d(&tA, d.A, BF, 2, d.a_rows, d.K, g2::BM) &&
-            tma_encode_3d(&tB, d.B, BF, 2, d.n_experts > 0 ? d.n_experts : d.E, d.b_rows, d.K, g2::BNH) &&
-            tma_encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, g2::BNH);
+            tma_encode_3d(&tB, d.B, BF, 2, G, d.b_rows, d.K, g2::BNH) &&
+            tma_encode_3d(&tBs, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, g2::BNH) &&
+            tma_encode_3d(&tB64, d.B, BF, 2, G, d.b_rows, d.K, g2::BNH / 2) &&
+            tma_encode_3d(&tBs64, d.Bs ? d.Bs : d.B, BF, 2, 1, d.b_rows, d.K, g2::BNH / 2);
   if (!ok) {
     *err = "cuTensorMapEncodeTiled rejected a grouped-GEMM operand";
     return cudaErrorInvalidValue;
@@ -338,7 +370,7 @@ cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t
   a.status = d.status;
   a.wait_limit = 4000000000LL;  // about two seconds of SM clock
   cfg.gridDim = dim3(2 * max_pairs);
-  e = cudaLaunchKernelEx(&cfg, g2::grouped_gemm_bf16_pair_kernel, tA, tB, tBs, a);
+  e = cudaLaunchKernelEx(&cfg, g2::grouped_gemm_bf16_pair_kernel, tA, tB, tBs, tB64, tBs64, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

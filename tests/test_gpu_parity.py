@@ -45,7 +45,10 @@ SMALL = {
     "fp4_large_groups": _W["dsv3_decode_fp4"].replace(name="fp4_large_groups", T=2200, h=512, E=8, k=4,
                                                       n_group=2, topk_group=1, I=256, I_shared=256),
     "fp4_mixtral_large": _W["mixtral"].replace(name="fp4_mixtral_large", T=1100, h=256, I=256, dtype="nvfp4"),
-    # at least 1024 rows per expert on average: the bf16 expert GEMMs run on CTA pairs (256-row tiles)
+    # at least 128 rows per expert on average: the bf16 expert GEMMs run on CTA pairs (256-row tiles; a
+    # tail of at most 128 rows as a 128-row pair tile)
+    "pair_half_tiles": _W["dsv3_prefill"].replace(name="pair_half_tiles", T=600, h=512, E=16, k=4, n_group=4,
+                                                  topk_group=2, I=256, I_shared=256),
     "pair_mixtral": _W["mixtral"].replace(name="pair_mixtral", T=4500, h=512, I=384),
     "pair_dsv3": _W["dsv3_prefill"].replace(name="pair_dsv3", T=2600, h=512, E=8, k=4, n_group=2, topk_group=1,
                                             I=256, I_shared=256),
@@ -371,7 +374,7 @@ def test_routing_near_ties_bit_exact(score):
 def test_eplb_placement_matches_unplaced_layer(dtype, cf, pairs):
     """An EPLB placement (redundant replicas, card-major slots) only reorders the expert-major rows:
     the per-slot permutation matches the oracle and the layer output is bit-identical. With `pairs`
-    both layouts average over 1024 rows per slot, so the bf16 layers run the CTA-pair GEMMs."""
+    both layouts average over 128 rows per slot, so the bf16 layers run the CTA-pair GEMMs."""
     if pairs:
         base = synth.WORKLOADS["dsv3_decode"].replace(T=2600, h=512, E=8, k=4, n_group=2, topk_group=1, I=256,
                                                       I_shared=256, zipf_s=1.2, dtype=dtype, capacity_factor=cf)
