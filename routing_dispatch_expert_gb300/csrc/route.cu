@@ -146,29 +146,22 @@ cudaError_t launch_split_router_weight(const float* w, void* w3, int64_t n, cuda
 // ------------------------------------------------------------------------------------------
 namespace tk {
 
-// argmax over the warp: larger value wins, equal values go to the lower expert index
-__device__ __forceinline__ void warp_argmax(float& v, int& e, float& s) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    int oe = __shfl_xor_sync(0xffffffffu, e, o);
-    float os = __shfl_xor_sync(0xffffffffu, s, o);
-    if (ov > v || (ov == v && oe < e)) {
-      v = ov;
-      e = oe;
-      s = os;
-    }
-  }
+// Keys as order-preserving unsigned integers: a > b as floats <=> ord(a) > ord(b) (-0 is taken as +0;
+// NaN keys are replaced by -inf before). Every key maps above 0, so 0 marks "no candidate". A warp
+// argmax is then one redux.sync max plus a ballot: the lowest lane holding the maximum, and inside a
+// lane the lowest slot, is the lowest expert index among equal keys.
+__device__ __forceinline__ uint32_t ord(float f) {
+  const uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unord(uint32_t u) {
+  if (u == 0) return -INFINITY;
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_min(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
@@ -184,86 +177,134 @@ constexpr float kGroupGap = 2e-6f;  // between two group scores (sums of two key
 __device__ __forceinline__ float sigmoid_exact(float l) { return __double2float_rn(1.0 / (1.0 + exp(-(double)l))); }
 __device__ __forceinline__ float sigmoid_fast(float l) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l))); }
 
+// Per-lane constants of the expert slots: group index and validity, the same for every token.
+template <int EPL>
+struct Slots {
+  int grp[EPL];
+  bool valid[EPL];
+  float bias[EPL];
+  int lpg;  // lanes per group when every group is a whole number of lanes (else 0)
+};
+
 // Group stage and expert stage on the keys of one token. Returns in sel_e / sel_l (lanes < k) the
 // chosen experts in descending key order and their logits. *clear is false when a deciding gap is
 // below the thresholds (only tracked when track_gaps).
 template <int EPL>
-__device__ __forceinline__ void select_experts(const TopkDesc& d, const float (&key)[EPL], const float (&lv)[EPL],
-                                               const bool (&valid)[EPL], int lane, int gs, bool track_gaps,
-                                               int& sel_e, float& sel_l, bool& clear) {
+__device__ __forceinline__ void select_experts(const TopkDesc& d, const Slots<EPL>& sl, const float (&key)[EPL],
+                                               const float (&lv)[EPL], int lane, bool track_gaps, int& sel_e,
+                                               float& sel_l, bool& clear) {
   clear = true;
   uint32_t kept = 0xffffffffu;
   if (d.n_group > 1) {
+    // the score of group g (sum of its two best keys) ends in every lane of the group (lane-aligned
+    // groups) or in lane g
     float my_gscore = -INFINITY;
-    for (int g = 0; g < d.n_group; ++g) {
+    int my_group = -1;
+    if (sl.lpg) {
       float t1 = -INFINITY, t2 = -INFINITY;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const int e = lane * EPL + i;
-        if (valid[i] && e / gs == g) {
-          const float v = key[i];
-          if (v > t1) {
-            t2 = t1;
-            t1 = v;
-          } else if (v > t2) {
-            t2 = v;
-          }
+        const float v = key[i];
+        if (v > t1) {
+          t2 = t1;
+          t1 = v;
+        } else if (v > t2) {
+          t2 = v;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
+      for (int o = 1; o < sl.lpg; o <<= 1) {
         const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
         const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
         const float n1 = fmaxf(t1, o1);
         t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
         t1 = n1;
       }
-      const float sc = gs >= 2 ? __fadd_rn(t1, t2) : t1;
-      if (lane == g) my_gscore = sc;
+      my_gscore = EPL * sl.lpg >= 2 ? __fadd_rn(t1, t2) : t1;
+      my_group = sl.grp[0];
+    } else {
+      const int gs = d.E / d.n_group;
+      for (int g = 0; g < d.n_group; ++g) {
+        float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          if (sl.valid[i] && sl.grp[i] == g) {
+            const float v = key[i];
+            if (v > t1) {
+              t2 = t1;
+              t1 = v;
+            } else if (v > t2) {
+              t2 = v;
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+          const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+          const float n1 = fmaxf(t1, o1);
+          t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+          t1 = n1;
+        }
+        const float sc = gs >= 2 ? __fadd_rn(t1, t2) : t1;
+        if (lane == g) my_gscore = sc;
+      }
+      my_group = lane < d.n_group ? lane : -1;
     }
+    // the topk_group best groups, ties to the lower group index (lanes are in group order)
+    const uint32_t gu = my_group >= 0 ? ord(my_gscore) : 0u;
     kept = 0;
     for (int r = 0; r < d.topk_group; ++r) {
-      const bool cand = lane < d.n_group && !((kept >> lane) & 1u);
-      float v = cand ? my_gscore : -INFINITY;
-      int gi = cand ? lane : 64 + lane;
-      float dummy = 0.f;
-      warp_argmax(v, gi, dummy);
-      kept |= 1u << (gi & 31);
+      const bool cand = my_group >= 0 && !((kept >> my_group) & 1u);
+      const uint32_t u = cand ? gu : 0u;
+      const uint32_t m = __reduce_max_sync(0xffffffffu, u);
+      const uint32_t b = __ballot_sync(0xffffffffu, cand && u == m);
+      const int wl = __ffs(b) - 1;
+      kept |= 1u << __shfl_sync(0xffffffffu, my_group, wl);
     }
     if (track_gaps && d.topk_group < d.n_group) {
-      const bool in = lane < d.n_group && ((kept >> lane) & 1u);
-      const bool out = lane < d.n_group && !((kept >> lane) & 1u);
-      const float kept_min = warp_min(in ? my_gscore : INFINITY);
-      const float rest_max = warp_max(out ? my_gscore : -INFINITY);
+      const bool in = my_group >= 0 && ((kept >> my_group) & 1u);
+      const bool out = my_group >= 0 && !((kept >> my_group) & 1u);
+      const float kept_min = unord(__reduce_min_sync(0xffffffffu, in ? gu : 0xffffffffu));
+      const float rest_max = unord(__reduce_max_sync(0xffffffffu, out ? gu : 0u));
       if (!(kept_min - rest_max > kGroupGap)) clear = false;
     }
   }
-  uint32_t taken = 0;
+  uint32_t uk[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) uk[i] = (sl.valid[i] && ((kept >> sl.grp[i]) & 1u)) ? ord(key[i]) : 0u;
   sel_e = 0;
   sel_l = 0.f;
   float prev = 0.f;
   const int rounds = track_gaps ? d.k + 1 : d.k;  // one more round finds the best key left out
   for (int j = 0; j < rounds; ++j) {
-    float bv = -INFINITY, bl = 0.f;
-    int be = 0x7fffffff;
+    uint32_t lb = 0;
+    int li = 0;
+    float ll = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      const int e = lane * EPL + i;
-      const bool ok = valid[i] && !((taken >> i) & 1u) && ((kept >> (e / gs)) & 1u);
-      if (ok && (key[i] > bv || be == 0x7fffffff)) {
-        bv = key[i];
-        be = e;
-        bl = lv[i];
+      if (uk[i] > lb) {
+        lb = uk[i];
+        li = i;
+        ll = lv[i];
       }
     }
-    warp_argmax(bv, be, bl);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, lb);
+    const float bv = unord(m);
     if (track_gaps && j > 0 && !(prev - bv > kKeyGap)) clear = false;
     prev = bv;
     if (j == d.k) break;  // the (k+1)-th key only checks the gap
-    if (be / EPL == lane) taken |= 1u << (be - lane * EPL);
+    const uint32_t b = __ballot_sync(0xffffffffu, m != 0 && lb == m);
+    const int wl = b ? __ffs(b) - 1 : 0;
+    const int wi = __shfl_sync(0xffffffffu, li, wl);
+    const float wlv = __shfl_sync(0xffffffffu, ll, wl);
+    if (lane == wl && b) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (i == li) uk[i] = 0u;
+    }
     if (lane == j) {
-      sel_e = be;
-      sel_l = bl;
+      sel_e = b ? wl * EPL + wi : 0x7fffffff;
+      sel_l = wlv;
     }
   }
 }
@@ -272,35 +313,55 @@ template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int gs = d.E / d.n_group;
   const bool sigmoid = d.score == MOE_SCORE_SIGMOID;
+  const int gs = d.E / d.n_group;
+  Slots<EPL> sl;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane * EPL + i;
+    sl.valid[i] = e < d.E;
+    sl.grp[i] = sl.valid[i] ? e / gs : 0;
+    sl.bias[i] = (sigmoid && d.bias && sl.valid[i]) ? d.bias[e] : 0.f;
+  }
+  // groups made of whole lanes: every slot of a lane in one group, a power-of-two lane count per group
+  const int lpg_c = gs / EPL;
+  sl.lpg = (d.E == 32 * EPL && gs % EPL == 0 && lpg_c >= 1 && (lpg_c & (lpg_c - 1)) == 0) ? lpg_c : 0;
+  const bool vec = EPL % 4 == 0 && d.E == 32 * EPL && (reinterpret_cast<uintptr_t>(d.logits) & 15) == 0;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.T; t += warps) {
     const float* lrow = d.logits + (int64_t)t * d.E;
-    float key[EPL], lv[EPL], bias[EPL];
-    bool valid[EPL];
+    float key[EPL], lv[EPL];
+    if (vec) {
+#pragma unroll
+      for (int i = 0; i < EPL; i += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(lrow + lane * EPL + i);
+        lv[i] = q.x;
+        lv[i + 1] = q.y;
+        lv[i + 2] = q.z;
+        lv[i + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) lv[i] = sl.valid[i] ? lrow[lane * EPL + i] : 0.f;
+    }
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      const int e = lane * EPL + i;
-      valid[i] = e < d.E;
-      lv[i] = valid[i] ? lrow[e] : 0.f;
-      bias[i] = (sigmoid && d.bias && valid[i]) ? d.bias[e] : 0.f;
-      float kv = sigmoid ? __fadd_rn(sigmoid_fast(lv[i]), bias[i]) : lv[i];
+      float kv = sigmoid ? __fadd_rn(sigmoid_fast(lv[i]), sl.bias[i]) : lv[i];
       if (kv != kv) kv = -INFINITY;  // NaN never wins
-      key[i] = valid[i] ? kv : -INFINITY;
+      key[i] = sl.valid[i] ? kv : -INFINITY;
     }
     int sel_e;
     float sel_l;
     bool clear;
-    select_experts<EPL>(d, key, lv, valid, lane, gs, sigmoid, sel_e, sel_l, clear);
+    select_experts<EPL>(d, sl, key, lv, lane, sigmoid, sel_e, sel_l, clear);
     if (sigmoid && !clear) {
       // a near tie: decide on the exact keys
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        float kv = __fadd_rn(sigmoid_exact(lv[i]), bias[i]);
+        float kv = __fadd_rn(sigmoid_exact(lv[i]), sl.bias[i]);
         if (kv != kv) kv = -INFINITY;
-        key[i] = valid[i] ? kv : -INFINITY;
+        key[i] = sl.valid[i] ? kv : -INFINITY;
       }
-      select_experts<EPL>(d, key, lv, valid, lane, gs, false, sel_e, sel_l, clear);
+      select_experts<EPL>(d, sl, key, lv, lane, false, sel_e, sel_l, clear);
     }
 
     // route weights
@@ -324,12 +385,12 @@ __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
       float lmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (valid[i]) lmax = fmaxf(lmax, lv[i]);
+        if (sl.valid[i]) lmax = fmaxf(lmax, lv[i]);
       lmax = warp_max(lmax);
       double z = 0.0;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (valid[i]) z += exp((double)lv[i] - (double)lmax);
+        if (sl.valid[i]) z += exp((double)lv[i] - (double)lmax);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
       if (lane < d.k) w = exp((double)sel_l - (double)lmax) / z;

@@ -330,17 +330,24 @@ def test_fp8_weight_quantiser_is_bit_exact():
     assert s[1, 0, 0].item() == 1.0
 
 
-@pytest.mark.parametrize("score", ["sigmoid", "softmax"])
-def test_routing_near_ties_bit_exact(score):
+@pytest.mark.parametrize("score,E,G,Gk,k", [
+    ("sigmoid", 256, 8, 4, 8),  # groups of whole lanes (4 lanes of 8 experts)
+    ("sigmoid", 64, 4, 2, 8),  # 8 lanes of 2 experts per group
+    ("sigmoid", 96, 8, 3, 8),  # 3 experts per lane, 4 lanes per group
+    ("sigmoid", 160, 5, 2, 8),  # groups that split a lane: the general group stage
+    ("sigmoid", 32, 4, 2, 4),  # one expert per lane
+    ("softmax", 256, 1, 1, 8),
+    ("softmax", 8, 1, 1, 2),
+])
+def test_routing_near_ties_bit_exact(score, E, G, Gk, k):
     """Logits built to sit on decision boundaries (exact duplicates, neighbouring fp32 values, nearly
     equal group scores) route exactly as the oracle routes them."""
     rng = np.random.default_rng(21)
-    T, E, k = 4096, 256, 8
-    G, Gk = (8, 4) if score == "sigmoid" else (1, 1)
+    T = 4096
     logits = rng.standard_normal((T, E)).astype(np.float32) * 2
     for t in range(T):
         kind = t % 4
-        a = rng.choice(E, 12, replace=False)
+        a = rng.choice(E, min(12, E), replace=False)
         if kind == 0:  # exact duplicates around the selection boundary
             logits[t, a] = logits[t, a[0]]
         elif kind == 1:  # neighbouring fp32 values
