@@ -14,7 +14,10 @@
 // promote it: acc += partial * sa[row, kb] * sb[n_block, kb], in fp32 registers (64 per thread; four
 // warps share each TMEM lane quarter, one per quarter of the columns; two accumulators per packed
 // IEEE fma of a float2). The MMA of block kb+1 overlaps the promotion of block kb; four promotion
-// warps per SM sub-partition hide the TMEM-load latency. The partial is read 8 columns at a time so
+// warps per SM sub-partition hide the TMEM-load latency. The scales reach the promotion warps through
+// shared memory: a loader warp fetches them 8 K blocks at a time into a 16-slot ring ahead of use,
+// because a global load in the promotion loop waits for DRAM (the activation scales of a large batch
+// are evicted from L2 by the streaming weights) on every K block. The partial is read 8 columns at a time so
 // that 64 accumulators plus the loaded values fit the 96 registers a 576-thread CTA allows without
 // spilling (spilled values compete with the 192 KB TMA ring for the SM's L1), and the TMEM buffer is
 // handed back as soon as its last columns are in registers.
@@ -22,7 +25,8 @@
 //     the 128-column amax of H is shared by the four warps of a row through shared memory and a
 //     bounded mbarrier (never a blocking bar.sync, so a timed-out warp cannot hang the others).
 //   * persistent, one CTA per SM, 4-stage TMA ring of 48 KB (A 128 x 128 B, B 256 x 128 B), every
-//     wait bounded, the same exit path as the bf16 kernel.
+//     wait bounded, the same exit path as the bf16 kernel; warps: 0 TMA, 1 MMA, 2-17 promotion and
+//     epilogue, 18 scale loader.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -42,7 +46,10 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 16;
 constexpr int PARTS = EPI_WARPS / 4;  // column parts per TMEM lane quarter
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int SCALE_WARP = 2 + EPI_WARPS;  // stages the scales of each K block into shared memory
+constexpr int THREADS = 64 + 32 * EPI_WARPS + 32;
+constexpr int SRING = 16;  // K blocks of scales in the shared-memory ring
+constexpr int SCHUNK = 8;  // K blocks the scale loader fetches at once
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 
@@ -61,9 +68,20 @@ struct Args {
   long long wait_limit;
 };
 
+// The scales of one K block of a tile: the A scale of each of its 128 rows and the B scale of each
+// of its two 128-column blocks (mode 0: the gate block, the up block; mode 1: columns [0, 128) and
+// [128, 256)).
+struct ScaleSlot {
+  float a[BM];
+  float b[2];
+  float pad[2];
+};
+
 struct Shared {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
+  uint64_t sfull[SRING];
+  uint64_t sempty[SRING];
   uint64_t pfull[2];
   uint64_t pempty[2];
   uint64_t xchg;
@@ -71,6 +89,7 @@ struct Shared {
   uint32_t tmem_slot;
   volatile int abort_flag;
   float amax[2][PARTS][BM];  // [tile parity][column part][row]
+  ScaleSlot sc[SRING];
   grp::Table tb;
 };
 
@@ -97,6 +116,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(&s.pempty[i], EPI_WARPS);
       }
       mbar_init(&s.xchg, EPI_WARPS);
+      for (int i = 0; i < SRING; ++i) {
+        mbar_init(&s.sfull[i], 32);
+        mbar_init(&s.sempty[i], EPI_WARPS);
+      }
       mbar_init(&s.mma_done, 1);
       s.abort_flag = 0;
       fence_mbar_init();
@@ -187,6 +210,65 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     umma_commit(&s.mma_done);
     grp::drain_wait(&s.mma_done, 0, args.wait_limit);
+  } else if (warp == SCALE_WARP) {
+    // ---------------- scale loader: the scales of SCHUNK K blocks at a time into the ring, so that
+    // the promotion warps read them from shared memory instead of waiting on global loads (the
+    // activation scales of a large batch do not stay in L2 next to the streaming weights)
+    const int KB = kblocks;
+    const int R_tot = args.R + (args.shared ? args.T : 0);
+    const bool vec = (KB & 3) == 0 && (reinterpret_cast<uintptr_t>(args.a_scales) & 15) == 0;
+    int q = 0;
+    uint32_t qphase = 0;
+    bool fine = true;
+    for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
+      const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      const float* bsc = t.g < args.E ? args.b_scales : args.bs_scales;
+      const int gbase = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) * args.nb * KB : 0;
+      const int nb0 = args.mode == 0 ? t.n_tile : t.n_tile * 2;
+      const int nb1 = args.mode == 0 ? args.I / 128 + t.n_tile : t.n_tile * 2 + 1;
+      const float* bl = bsc + gbase + (lane == 0 ? nb0 : nb1) * KB;
+      const float* ar[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ar[i] = args.a_scales + (int64_t)min(t.a_row + lane + 32 * i, R_tot - 1) * KB;
+      for (int kc = 0; kc < KB && fine; kc += SCHUNK) {
+        const int n = min(SCHUNK, KB - kc);
+        float av[4][SCHUNK], bv[SCHUNK];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (vec && n == SCHUNK) {
+            const float4 u = *reinterpret_cast<const float4*>(ar[i] + kc);
+            const float4 w = *reinterpret_cast<const float4*>(ar[i] + kc + 4);
+            av[i][0] = u.x, av[i][1] = u.y, av[i][2] = u.z, av[i][3] = u.w;
+            av[i][4] = w.x, av[i][5] = w.y, av[i][6] = w.z, av[i][7] = w.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < SCHUNK; ++j) av[i][j] = j < n ? ar[i][kc + j] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < SCHUNK; ++j) bv[j] = (lane < 2 && j < n) ? bl[kc + j] : 0.f;
+#pragma unroll
+        for (int j = 0; j < SCHUNK; ++j) {
+          if (j >= n) break;
+          int ok = 1;
+          if (lane == 0) ok = wait_or_abort(&s.sempty[q], qphase ^ 1, &s.abort_flag, args.status, args.wait_limit);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            fine = false;
+            break;
+          }
+          __syncwarp();  // the slot is free for every lane, not only the one that waited
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s.sc[q].a[lane + 32 * i] = av[i][j];
+          if (lane < 2) s.sc[q].b[lane] = bv[j];
+          mbar_arrive(&s.sfull[q]);
+          if (++q == SRING) {
+            q = 0;
+            qphase ^= 1;
+          }
+        }
+      }
+    }
   } else if (warp >= 2) {
     // ---------------- promotion + epilogue (16 warps)
     const int quarter = warp & 3;
@@ -198,37 +280,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tq = tmem_base + ((uint32_t)(quarter * 32) << 16);  // this warp's TMEM lane quarter
     const uint32_t tqa = tq + (uint32_t)col_a, tqb = tq + (uint32_t)col_b;
     const int KB = kblocks;
-    const int R_tot = args.R + (args.shared ? args.T : 0);
     int p = 0, tpar = 0;
     uint32_t pphase = 0, xphase = 0;
     bool fine = true;
+    // column block of this thread's scales: mode 0 gate (block 0) and up (block 1); mode 1 the block
+    // holding its 64 columns
+    const int blo = args.mode == 0 ? 0 : part >> 1;
+    const int bhi = args.mode == 0 ? 1 : part >> 1;
+    int q = 0;
+    uint32_t qphase = 0;
     for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
-      // scale pointers of this tile (32-bit indices: R_tot * K/128 and E * nb * K/128 stay far below
-      // 2^31); rows past the buffer read the last row's scales and are never stored
-      const float* sar;
-      const float* sbl;
-      const float* sbh;
-      {
-        const grp::Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
-        const float* bsc = t.g < args.E ? args.b_scales : args.bs_scales;
-        const int gbase = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) * args.nb * KB : 0;
-        const int nb_lo = args.mode == 0 ? t.n_tile : t.n_tile * 2 + (part >> 1);
-        const int nb_hi = args.mode == 0 ? args.I / 128 + t.n_tile : nb_lo;
-        sar = args.a_scales + min(t.a_row + r, R_tot - 1) * KB;
-        sbl = bsc + gbase + nb_lo * KB;
-        sbh = bsc + gbase + nb_hi * KB;
-      }
-
       // acc[i] holds columns (2i, 2i+1) of this thread's 64: [0, 16) the col_a block, [16, 32) col_b
       float2 acc[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
-      float sa_n = sar[0];  // the row scale is prefetched one K block ahead
       for (int kb = 0; kb < KB; ++kb) {
-        const float s_lo = sa_n * sbl[kb], s_hi = sa_n * sbh[kb];
-        sa_n = sar[min(kb + 1, KB - 1)];
-        const float2 slo = make_float2(s_lo, s_lo), shi = make_float2(s_hi, s_hi);
         int ok = 1;
+        if (lane == 0) ok = wait_or_abort(&s.sfull[q], qphase, &s.abort_flag, args.status, args.wait_limit);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          fine = false;
+          break;
+        }
+        __syncwarp();
+        // the scales of this K block (rows past the buffer carry the last row's scale and are never
+        // stored); the slot is handed back once they are in registers
+        const float sa = s.sc[q].a[r];
+        const float s_lo = sa * s.sc[q].b[blo], s_hi = sa * s.sc[q].b[bhi];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sempty[q]);
+        if (++q == SRING) {
+          q = 0;
+          qphase ^= 1;
+        }
+        const float2 slo = make_float2(s_lo, s_lo), shi = make_float2(s_hi, s_hi);
         if (lane == 0) ok = wait_or_abort(&s.pfull[p], pphase, &s.abort_flag, args.status, args.wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
