@@ -263,6 +263,44 @@ def config_of(wl, world):
             "l2": "inputs larger than L2: every step reads all active expert weights (GBs) once"}
 
 
+def measure_fp8_peak(n=8192, sustain_s=4.0):
+    """Dense e4m3 GEMM rate of the vendor library on this GPU, the way the bf16 peak is measured:
+    best of 10 n^3 products (burst) and back to back for a few seconds (sustained), 2 n^3 FLOPs each,
+    tensor-wise fp32 scales, bf16 out. Context for the FP8 roofline, which uses the measured bf16
+    peak times the nominal FP8/bf16 ratio of 2."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = (torch.randn(n, n, device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
+    b = (torch.randn(n, n, device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
+    one = torch.ones((), device=dev, dtype=torch.float32)
+    f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        f()
+        e.record()
+        torch.cuda.synchronize()
+        best = min(best, s.elapsed_time(e))
+    flops = 2.0 * n ** 3
+    reps = max(10, int(sustain_s * 1e3 / best))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        f()
+    e.record()
+    torch.cuda.synchronize()
+    sus = s.elapsed_time(e) / reps
+    print(json.dumps({"fp8_e4m3_tflops": flops / best / 1e9, "fp8_e4m3_tflops_sustained": flops / sus / 1e9,
+                      "n": n, "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, tensor-wise scales; best of 10 "
+                                     f"(burst) and {reps} back to back (sustained)"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -273,9 +311,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None, help="override T (small profiling cases)")
     ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
+    ap.add_argument("--fp8-peak", action="store_true",
+                    help="measure the library FP8 GEMM rate (cuBLASLt through torch._scaled_mm) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.fp8_peak:
+        measure_fp8_peak()
+        return
 
     import synth
 
@@ -418,18 +461,48 @@ def main():
     ms_graph = g_s.elapsed_time(g_e) / args.steps
     del graph
 
-    # end to end through the public API with host buffers: pinned x in, y out, every step
+    # end to end through the public API with host buffers: every step copies its x in from pinned host
+    # memory and its y out to pinned host memory. The copies run on their own streams with two device
+    # buffers of x and y alternating, so the copy-in of step i+1 and the copy-out of step i-1 overlap
+    # the layer of step i (the way a serving loop feeds a layer).
     x_host = x.cpu().pin_memory()
-    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    x_dev = torch.empty_like(x)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, args.steps // 2)
+    y_host = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    y_dev = [y, torch.empty_like(y)]
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]  # x_dev[b] holds the step's input
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the layer has read x_dev[b] and written y_dev[b]
+    ev_out = [torch.cuda.Event() for _ in range(2)]  # y_dev[b] is on the host
+
+    def e2e_step(i):
+        b = i & 1
+        if i >= 2:
+            h2d.wait_event(ev_used[b])
+        with torch.cuda.stream(h2d):
+            x_dev[b].copy_(x_host, non_blocking=True)
+        ev_in[b].record(h2d)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])
+        rde.forward(cfg, x_dev[b], weights, y_dev[b], ws)
+        ev_used[b].record(stream)
+        d2h.wait_event(ev_used[b])
+        with torch.cuda.stream(d2h):
+            y_host[b].copy_(y_dev[b], non_blocking=True)
+        ev_out[b].record(d2h)
+
+    e2e_steps = max(4, args.steps // 2)
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_s.record(stream)
-    for _ in range(e2e_steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        rde.forward(cfg, x_dev, weights, y, ws)
-        y_host.copy_(y, non_blocking=True)
+    h2d.wait_stream(stream)
+    d2h.wait_stream(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_event(ev_out[0])
+    stream.wait_event(ev_out[1])
     e_e.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = e_s.elapsed_time(e_e) / e2e_steps
