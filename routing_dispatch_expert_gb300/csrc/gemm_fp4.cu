@@ -226,12 +226,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool fine = true;
     for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
       for (int kb = 0; kb < kblocks; ++kb) {
-        int ok = 1;
-        if (lane == 0)
-          ok = wait_or_abort(&s.qfull[stage], phase, &s.abort_flag, args.status, args.wait_limit) &&
-               wait_or_abort(&s.bempty[bst], bphase ^ 1, &s.abort_flag, args.status, args.wait_limit);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
+        // every lane polls the barriers itself (cheaper than a lane-0 wait and a broadcast)
+        const int ok = wait_or_abort(&s.qfull[stage], phase, &s.abort_flag, args.status, args.wait_limit) &&
+                       wait_or_abort(&s.bempty[bst], bphase ^ 1, &s.abort_flag, args.status, args.wait_limit);
+        if (__any_sync(0xffffffffu, !ok)) {
           fine = false;
           break;
         }

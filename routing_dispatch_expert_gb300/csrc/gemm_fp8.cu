@@ -295,10 +295,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
       for (int kb = 0; kb < KB; ++kb) {
-        int ok = 1;
-        if (lane == 0) ok = wait_or_abort(&s.sfull[q], qphase, &s.abort_flag, args.status, args.wait_limit);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
+        // every lane polls the barrier itself: a lane-0 wait followed by a broadcast costs ~7% of the
+        // FFN on this per-K-block hand-off
+        int ok = wait_or_abort(&s.sfull[q], qphase, &s.abort_flag, args.status, args.wait_limit);
+        if (__any_sync(0xffffffffu, !ok)) {
           fine = false;
           break;
         }
@@ -314,9 +314,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           qphase ^= 1;
         }
         const float2 slo = make_float2(s_lo, s_lo), shi = make_float2(s_hi, s_hi);
-        if (lane == 0) ok = wait_or_abort(&s.pfull[p], pphase, &s.abort_flag, args.status, args.wait_limit);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
+        ok = wait_or_abort(&s.pfull[p], pphase, &s.abort_flag, args.status, args.wait_limit);
+        if (__any_sync(0xffffffffu, !ok)) {
           fine = false;
           break;
         }
