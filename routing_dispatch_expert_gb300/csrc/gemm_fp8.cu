@@ -113,12 +113,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.pfull[i], 1);
-        mbar_init(&s.pempty[i], EPI_WARPS);
+        mbar_init(&s.pempty[i], 32 * EPI_WARPS);
       }
       mbar_init(&s.xchg, EPI_WARPS);
       for (int i = 0; i < SRING; ++i) {
         mbar_init(&s.sfull[i], 32);
-        mbar_init(&s.sempty[i], EPI_WARPS);
+        mbar_init(&s.sempty[i], 32 * EPI_WARPS);
       }
       mbar_init(&s.mma_done, 1);
       s.abort_flag = 0;
@@ -307,8 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // stored); the slot is handed back once they are in registers
         const float sa = s.sc[q].a[r];
         const float s_lo = sa * s.sc[q].b[blo], s_hi = sa * s.sc[q].b[bhi];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.sempty[q]);
+        mbar_arrive(&s.sempty[q]);
         if (++q == SRING) {
           q = 0;
           qphase ^= 1;
@@ -330,8 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (g == 7) {
             // the partial is in registers: hand the TMEM buffer back before the last multiply-adds
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.pempty[p]);
+            mbar_arrive(&s.pempty[p]);  // every lane arrives (the barrier counts 32 per warp)
           }
 #pragma unroll
           for (int i = 0; i < 4; ++i)
