@@ -237,6 +237,13 @@ int moe_combine(const moe_config* cfg, const void* yd, const int32_t* inv_pos, v
 
 /* The whole layer: route -> dispatch -> experts -> combine, intermediates in ws (their places
  * are given by moe_workspace_layout). x [T, h] bf16 in, y [T, h] bf16 out.
+ * bf16 layers with a shared expert run it on a second stream (TensorRT-LLM "DeepSeek R1 throughput
+ * on Blackwell", multi-stream: it needs only x): the call records an event on `stream` after routing,
+ * enqueues the shared expert (rows read from x, written to rows [T*k, T*k + T) of hbuf and yd) on a
+ * library-owned stream of the current device (created with two events on first use, kept for the
+ * life of the process), and makes `stream` wait for it before the combine. Work enqueued on `stream`
+ * after the call therefore sees the whole layer, and the call can be captured into a CUDA graph on
+ * `stream`; the routed rows of xd are the only ones dispatch writes on this path.
  * Errors: as the steps above. */
 int moe_forward(const moe_config* cfg, const void* x, const moe_weights* weights, void* y, void* ws,
                 size_t ws_bytes, moe_stream_t stream);

@@ -216,7 +216,7 @@ int capacity_of(const moe_config* c) {
 
 int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, const float* topk_w, int32_t* counts,
                 int32_t* offsets, int32_t* inv_pos, int32_t* row_token, float* row_weight, void* xd, float* xd_scales,
-                void* ws, const Layout& L, cudaStream_t stream) {
+                void* ws, const Layout& L, cudaStream_t stream, bool shared_rows = true) {
   moe::DispatchDesc d;
   d.x = x;
   d.topk_idx = topk_idx;
@@ -234,7 +234,7 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   d.h = c->h;
   d.E = c->E;
   d.k = c->k;
-  d.shared = c->I_shared > 0;
+  d.shared = c->I_shared > 0 && shared_rows;  // false: the shared expert reads x itself
   d.fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
   d.capacity = capacity_of(c);
   set_placement(d, c, expert_counts_ptr(ws, L.l, c));
@@ -256,9 +256,9 @@ bool use_pair_tiles(const moe_config* c, int S) {
 
 int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, const float* xd_scales,
                   const int32_t* offsets, const float* row_weight, void* yd, void* ws, const Layout& L,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool with_shared = true) {
   if (c->T == 0) return MOE_OK;
-  const bool shared = c->I_shared > 0;
+  const bool shared = c->I_shared > 0 && with_shared;
   std::string err;
   const int S = (int)n_groups(c);
   const int32_t* slot_expert = c->placement ? c->placement->slot_expert : nullptr;
@@ -394,6 +394,58 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
   return MOE_OK;
 }
 
+// The shared expert alone (bf16): a dense SwiGLU MLP over all T tokens (inference guide 6.4 section 7:
+// every token uses it, weight 1), as one group whose rows are read straight from x; it writes rows
+// [R, R + T) of hbuf and yd, where the combine expects them. moe_forward runs it on a second stream
+// while the routed rows are dispatched (TensorRT-LLM "DeepSeek R1 throughput on Blackwell",
+// multi-stream: the shared expert does not depend on the routing).
+int do_shared_ffn_bf16(const moe_config* c, const moe_weights* w, const void* x, void* ws, const Layout& L,
+                       cudaStream_t stream) {
+  if (c->T == 0) return MOE_OK;
+  std::string err;
+  // the kernel the shared group would get inside the routed launch, so that both paths compute its
+  // rows with the same tiles (bit-identical outputs)
+  auto launch = use_pair_tiles(c, (int)n_groups(c)) ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
+  __nv_bfloat16* hs = at<__nv_bfloat16>(ws, L.l.hbuf) + L.R * (int64_t)c->I;
+  __nv_bfloat16* ys = at<__nv_bfloat16>(ws, L.l.yd) + L.R * (int64_t)c->h;
+  moe::GroupedGemmDesc g;
+  g.slot_expert = nullptr;
+  g.n_experts = 1;
+  g.A = x;
+  g.a_rows = c->T;
+  g.B = w->w_gu_shared;
+  g.Bs = w->w_gu_shared;
+  g.b_rows = 2 * (int64_t)c->I;
+  g.offsets = nullptr;  // one group: rows [0, T)
+  g.E = 0;
+  g.R = 0;
+  g.T = c->T;
+  g.K = c->h;
+  g.N = 2 * c->I;
+  g.I = c->I;
+  g.mode = 0;
+  g.out = hs;
+  g.ldo = c->I;
+  g.row_weight = nullptr;
+  g.status = status_ptr(ws, L.l);
+  cudaError_t e = launch(g, stream, &err);
+  if (e != cudaSuccess)
+    return err.empty() ? cuda_fail(e, "shared-expert gate/up launch") : cuda_fail(e, err.c_str());
+  g.A = hs;
+  g.B = w->w_d_shared;
+  g.Bs = w->w_d_shared;
+  g.b_rows = c->h;
+  g.K = c->I;
+  g.N = c->h;
+  g.mode = 1;
+  g.out = ys;
+  g.ldo = c->h;
+  e = launch(g, stream, &err);
+  if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "shared-expert down launch") : cuda_fail(e, err.c_str());
+  counted(2);
+  return MOE_OK;
+}
+
 int check_expert_weights(const moe_config* c, const moe_weights* w) {
   if (!w) return fail(MOE_ERR_INVALID, "weights is NULL");
   REQUIRE_PTR(w->w_gu, "weights->w_gu");
@@ -516,6 +568,36 @@ MOE_EXPORT int moe_combine(const moe_config* cfg, const void* yd, const int32_t*
   return MOE_OK;
 }
 
+namespace {
+
+// A second stream per device for the shared expert, with the fork and join events. Created on first
+// use and kept for the life of the process; the enqueue of a fork ... join section holds the mutex,
+// so calls from several host threads cannot interleave their event records.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream& sd = g_side[dev];
+  if (!sd.stream) {
+    if ((e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &sd;
+  return cudaSuccess;
+}
+
+}  // namespace
+
 MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weights* weights, void* y, void* ws,
                            size_t ws_bytes, moe_stream_t stream) {
   int rc = check_config(cfg);
@@ -534,13 +616,41 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   if ((rc = do_route(cfg, x, weights, at<float>(ws, l.logits), 0, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w),
                      ws, L, s)))
     return rc;
+  // bf16 layers with a shared expert: the shared expert runs on a second stream from here on (it
+  // needs only x), overlapping dispatch and the routed GEMMs; the combine waits for it
+  const bool side = cfg->I_shared > 0 && cfg->T > 0 && cfg->dtype == MOE_DTYPE_BF16;
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  SideStream* sd = nullptr;
+  if (side) {
+    side_lock.lock();
+    if ((e = side_stream(&sd)) != cudaSuccess) return cuda_fail(e, "second stream set-up");
+    if ((e = cudaEventRecord(sd->fork, s)) != cudaSuccess) return cuda_fail(e, "fork event record");
+    if ((e = cudaStreamWaitEvent(sd->stream, sd->fork, 0)) != cudaSuccess) return cuda_fail(e, "fork wait");
+    const int src = do_shared_ffn_bf16(cfg, weights, x, ws, L, sd->stream);
+    // the join is recorded even after a failed launch, so that a capture on `s` can still end
+    if ((e = cudaEventRecord(sd->join, sd->stream)) != cudaSuccess) return cuda_fail(e, "join event record");
+    if (src) {
+      cudaStreamWaitEvent(s, sd->join, 0);
+      return src;
+    }
+  }
   if ((rc = do_dispatch(cfg, x, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w), at<int32_t>(ws, l.counts),
                         at<int32_t>(ws, l.offsets), at<int32_t>(ws, l.inv_pos), at<int32_t>(ws, l.row_token),
-                        at<float>(ws, l.row_weight), at<void>(ws, l.xd), at<float>(ws, l.xd_scales), ws, L, s)))
+                        at<float>(ws, l.row_weight), at<void>(ws, l.xd), at<float>(ws, l.xd_scales), ws, L, s,
+                        !side))) {
+    if (side) cudaStreamWaitEvent(s, sd->join, 0);
     return rc;
+  }
   if ((rc = do_expert_ffn(cfg, weights, at<void>(ws, l.xd), at<float>(ws, l.xd_scales), at<int32_t>(ws, l.offsets),
-                          at<float>(ws, l.row_weight), at<void>(ws, l.yd), ws, L, s)))
+                          at<float>(ws, l.row_weight), at<void>(ws, l.yd), ws, L, s, !side))) {
+    if (side) cudaStreamWaitEvent(s, sd->join, 0);
     return rc;
+  }
+  if (side) {
+    // the join wait is enqueued before the lock is released: it binds the record of this call
+    if ((e = cudaStreamWaitEvent(s, sd->join, 0)) != cudaSuccess) return cuda_fail(e, "join wait");
+    side_lock.unlock();
+  }
   e = moe::launch_combine(at<void>(ws, l.yd), at<int32_t>(ws, l.inv_pos), y, cfg->T, cfg->h, cfg->k,
                           cfg->I_shared > 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");

@@ -116,7 +116,7 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
     else:
         xd = bits(it["xd"])
         np.testing.assert_array_equal(xd[:Rk], ref["xd"])
-        if wl.has_shared:
+        if wl.has_shared and wl.dtype != "bf16":  # bf16: the shared expert reads x itself
             np.testing.assert_array_equal(xd[R:], x)
 
     # expert outputs per row (route-weighted), and the shared expert's rows
@@ -192,7 +192,10 @@ def test_steps_through_their_own_entry_points():
     for a, b in ((counts, "counts"), (offsets, "offsets"), (inv_pos, "inv_pos"), (row_token, "row_token"),
                  (row_weight, "row_weight")):
         assert torch.equal(a, it[b]), b
-    assert torch.equal(xd.view(torch.int16), it["xd"].view(torch.int16))
+    R = T * k
+    assert torch.equal(xd[:R].view(torch.int16), it["xd"][:R].view(torch.int16))
+    # the step entry point copies the shared expert's rows; moe_forward's shared expert reads x itself
+    assert torch.equal(xd[R:].view(torch.int16), L.inp["x"].view(torch.int16))
     yd = torch.empty(R_tot, h, dtype=torch.bfloat16, device=dev)
     rde.expert_ffn(cfg, L.weights, xd, None, offsets, row_weight, yd, ws)
     assert torch.equal(yd.view(torch.int16), it["yd"].view(torch.int16))
@@ -214,7 +217,7 @@ def test_combine_identity_experts_closed_form():
     xd = it["xd"].float()
     yd = torch.empty_like(it["yd"])
     yd[:R] = (xd[:R] * it["row_weight"][:, None]).to(torch.bfloat16)
-    yd[R:] = it["xd"][R:]
+    yd[R:] = L.inp["x"]
     y = torch.empty_like(L.inp["x"])
     rde.combine(L.cfg, yd, it["inv_pos"], y)
     torch.cuda.synchronize()
