@@ -23,11 +23,14 @@ namespace moe {
 // ------------------------------------------------------------------------------------------
 // router GEMM for small E (E < 128, or E not a multiple of 32): logits[T, E] = x[T, h] . w_r[E, h]^T
 // on the CUDA cores in fp32. The output is only E columns wide, so the work is split over tokens and K
-// instead of output tiles: a CTA of 8 warps takes TPW tokens and EMAX experts (blockIdx.y selects the
-// expert block when E > 64); warp w takes the 256-element K chunks
-// w, w + 8, ... (each lane 8 consecutive elements of a chunk: one 16-byte load of x per token, two
-// 16-byte loads of each expert's weight row, L1-resident); lanes are summed by a butterfly, the 8
-// warps' partial sums in warp order through shared memory (the same order on every run).
+// instead of output tiles: a CTA of 8 warps takes EMAX experts (blockIdx.y selects the expert block
+// when E > 64) and `groups` x TPW tokens. The warps form `groups` groups of kw = 8 / groups warps
+// (kw = 8 when h has at least 8 chunks of 256, else the largest power of two not above the chunk
+// count, so that no warp idles on a short row); warp j of a group takes that group's TPW tokens and
+// the 256-element K chunks j, j + kw, ... (each lane 8 consecutive elements of a chunk: one 16-byte
+// load of x per token, two 16-byte loads of each expert's weight row, L1-resident); lanes are summed
+// by a butterfly, the kw warps' partial sums in warp order through shared memory (the same order on
+// every run).
 // ------------------------------------------------------------------------------------------
 namespace rg {
 constexpr int WARPS = 8, THREADS = 32 * WARPS;
@@ -35,10 +38,12 @@ constexpr int WARPS = 8, THREADS = 32 * WARPS;
 template <int EMAX, int TPW>
 __global__ void __launch_bounds__(THREADS) router_small_e_kernel(const __nv_bfloat16* __restrict__ x,
                                                                  const float* __restrict__ w, float* __restrict__ out,
-                                                                 int T, int h, int E) {
+                                                                 int T, int h, int E, int kw) {
   __shared__ float part[WARPS][TPW][EMAX];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * TPW;
+  const int groups = WARPS / kw;
+  const int grp = warp / kw, kj = warp - grp * kw;
+  const int t0 = (blockIdx.x * groups + grp) * TPW;
   const int e0 = blockIdx.y * EMAX;
   const int ne = min(EMAX, E - e0);  // experts of this block
   float acc[TPW][EMAX];
@@ -47,7 +52,7 @@ __global__ void __launch_bounds__(THREADS) router_small_e_kernel(const __nv_bflo
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) acc[t][e] = 0.f;
   const int chunks = h / 256;
-  for (int c = warp; c < chunks; c += WARPS) {
+  for (int c = kj; c < chunks; c += kw) {
     const int k = c * 256 + lane * 8;
     float xv[TPW][8];
 #pragma unroll
@@ -84,13 +89,13 @@ __global__ void __launch_bounds__(THREADS) router_small_e_kernel(const __nv_bflo
       if (lane == 0) part[warp][t][e] = v;
     }
   __syncthreads();
-  for (int i = threadIdx.x; i < TPW * EMAX; i += THREADS) {
-    const int t = i / EMAX, e = i % EMAX;
-    if (e < ne && t0 + t < T) {
-      float v = part[0][t][e];
-#pragma unroll
-      for (int q = 1; q < WARPS; ++q) v += part[q][t][e];
-      out[(int64_t)(t0 + t) * E + e0 + e] = v;
+  for (int i = threadIdx.x; i < groups * TPW * EMAX; i += THREADS) {
+    const int g = i / (TPW * EMAX), t = (i / EMAX) % TPW, e = i % EMAX;
+    const int tok = (blockIdx.x * groups + g) * TPW + t;
+    if (e < ne && tok < T) {
+      float v = part[g * kw][t][e];
+      for (int q = 1; q < kw; ++q) v += part[g * kw + q][t][e];
+      out[(int64_t)tok * E + e0 + e] = v;
     }
   }
 }
@@ -100,9 +105,12 @@ cudaError_t launch_router_gemm(const void* x, const float* w_r, float* logits, i
                                cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
-#define RG_LAUNCH(EM, TP)                                                                               \
-  rg::router_small_e_kernel<EM, TP>                                                                    \
-      <<<dim3((unsigned)cdiv(T, TP), (unsigned)cdiv(E, EM)), rg::THREADS, 0, stream>>>(xb, w_r, logits, T, h, E)
+  const int chunks = h / 256;
+  const int kw = chunks >= rg::WARPS ? rg::WARPS : chunks >= 4 ? 4 : chunks >= 2 ? 2 : 1;
+  const int groups = rg::WARPS / kw;
+#define RG_LAUNCH(EM, TP)                                                                                     \
+  rg::router_small_e_kernel<EM, TP><<<dim3((unsigned)cdiv(T, (int64_t)TP * groups), (unsigned)cdiv(E, EM)), \
+                                      rg::THREADS, 0, stream>>>(xb, w_r, logits, T, h, E, kw)
   if (E <= 8)
     RG_LAUNCH(8, 4);
   else if (E <= 16)
@@ -382,6 +390,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
       continue;
     }
     {
+      // softmax probabilities: the exponentials in fp32 (at most 2 ulp, relative error below 3e-7
+      // with the rounding of l - lmax), summed and divided in fp64; the probabilities enter the
+      // combine, not a selection (fp64 exp costs ~15 us per launch on this part's slow fp64 pipe)
       float lmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
@@ -390,10 +401,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
       double z = 0.0;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (sl.valid[i]) z += exp((double)lv[i] - (double)lmax);
+        if (sl.valid[i]) z += (double)expf(lv[i] - lmax);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (lane < d.k) w = exp((double)sel_l - (double)lmax) / z;
+      if (lane < d.k) w = (double)expf(sel_l - lmax) / z;
     }
     if (d.renorm) {
       double sum = lane < d.k ? w : 0.0;
