@@ -73,6 +73,26 @@ struct Layout {
 // expert-major buffers are grouped per physical slot (one per expert without a placement)
 int64_t n_groups(const moe_config* c) { return c->placement ? c->placement->n_slots : c->E; }
 
+// The tensor-core router (E >= 128, E a multiple of 32) works on 128 x 128 output tiles; a batch with
+// fewer than 64 of them would leave most SMs idle for the whole K loop (T = 256, E = 256: 4 tiles, each
+// 336 K steps), so each tile's K range is split over several CTAs (at least 2 K blocks of 64 each, up
+// to about 128 CTAs in all) whose fp32 partial sums are added in a fixed order afterwards.
+bool tensor_core_router(const moe_config* c) { return c->E >= 128 && c->E % 32 == 0; }
+int router_csplit(const moe_config* c) {
+  if (!tensor_core_router(c) || c->T <= 0) return 1;
+  const int64_t tiles = moe::cdiv(c->T, 128) * moe::cdiv(c->E, 128);
+  if (tiles >= 64) return 1;
+  const int kpb = c->h / 64;
+  const int want = (int)std::min<int64_t>(kpb / 2, moe::cdiv(128, tiles));
+  if (want < 2) return 1;
+  const int kper = (kpb + want - 1) / want;
+  return (kpb + kper - 1) / kper;  // every split gets a non-empty K range
+}
+// bytes of the scratch region in front of the router's partial sums (status word, histograms)
+size_t scratch_core_bytes(const moe_config* c) {
+  return align256(256 + sizeof(int32_t) * (moe::dispatch_scratch_ints(c->T, c->E) + c->E));
+}
+
 Layout make_layout(const moe_config* c) {
   Layout L;
   const int64_t T = c->T, E = c->E, k = c->k, h = c->h, I = c->I, S = n_groups(c);
@@ -100,7 +120,8 @@ Layout make_layout(const moe_config* c) {
   l.h_scales = take(fp8 ? sizeof(float) * L.R_tot * (I / 128) : 0);
   l.yd = take(2 * L.R_tot * h);
   l.router_w3 = take(2 * 3 * E * h);
-  l.scratch = take(256 + sizeof(int32_t) * (moe::dispatch_scratch_ints(c->T, c->E) + E));
+  const int cs = router_csplit(c);
+  l.scratch = take(scratch_core_bytes(c) + (cs > 1 ? sizeof(float) * cs * T * E : 0));
   l.total = o;
   return L;
 }
@@ -148,8 +169,6 @@ int check_ws(void* ws, size_t ws_bytes, const Layout& L) {
     if (!aligned16(p)) return fail(MOE_ERR_INVALID, std::string(name) + " must be 16-byte aligned"); \
   } while (0)
 
-bool tensor_core_router(const moe_config* c) { return c->E >= 128 && c->E % 32 == 0; }
-
 int do_route(const moe_config* c, const void* x, const moe_weights* w, float* logits, int flags, int32_t* topk_idx,
              float* topk_w, void* ws, const Layout& L, cudaStream_t stream) {
   cudaError_t e;
@@ -174,13 +193,20 @@ int do_route(const moe_config* c, const void* x, const moe_weights* w, float* lo
       g.I = 0;
       g.mode = 2;
       g.ksplit = 3;
-      g.out = logits;
+      g.csplit = router_csplit(c);
+      float* partials = at<float>(ws, L.l.scratch + scratch_core_bytes(c));
+      g.out = g.csplit > 1 ? static_cast<void*>(partials) : static_cast<void*>(logits);
       g.ldo = c->E;
       g.row_weight = nullptr;
       g.status = status_ptr(ws, L.l);
       e = moe::launch_grouped_gemm_bf16(g, stream, &err);
       if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "router GEMM launch") : cuda_fail(e, err.c_str());
       counted(2);
+      if (g.csplit > 1) {
+        e = moe::launch_router_reduce(partials, logits, g.csplit, (int64_t)c->T * c->E, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "router partial-sum launch");
+        counted(1);
+      }
     } else {
       e = moe::launch_router_gemm(x, w->w_router, logits, c->T, c->h, c->E, stream);
       if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");

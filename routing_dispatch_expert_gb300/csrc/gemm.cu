@@ -13,7 +13,9 @@
 //           three bf16 terms [3, E, h]; x is exact in bf16 and every bf16 x bf16 product is exact in
 //           fp32. The tensor core's accumulator does not round like an IEEE fp32 add over thousands
 //           of steps, so the MMAs accumulate chunks of ROUTER_CHUNK K blocks in TMEM (double
-//           buffered, 128-column tiles) and the epilogue sums the chunks in fp32 registers.
+//           buffered, 128-column tiles) and the epilogue sums the chunks in fp32 registers. A batch
+//           too small to fill the SMs splits each tile's K range over `csplit` CTAs, which write fp32
+//           partial sums that launch_router_reduce adds in split order.
 // Work follows the device-side per-expert counts (Perplexity, "Quantization": kernels read the
 // routing information to split the work, instead of sizing it from buffer bounds), so the launch
 // needs no host read-back and has a fixed grid.
@@ -67,6 +69,8 @@ struct Args {
   int mode;     // 0: gate/up + SwiGLU -> H; 1: down * row_weight -> yd; 2: router, fp32 out
   int I;        // mode 0: row offset of the up half inside W_gu
   int ksplit;   // B is split into ksplit K passes over the same A (mode 2: 3), else 1
+  int csplit;   // mode 2: CTAs sharing one output tile, each over a contiguous range of K (1: none);
+                // split s writes its fp32 partial sums to out + s * T * ldo
   int n_valid;  // mode 2: output columns that exist (E)
   int ldo;      // output row stride in elements
   void* out;
@@ -128,9 +132,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_slot;
-  const int total = s.tb.gtile[G] * args.n_tiles;
+  const int csplit = args.mode == 2 ? args.csplit : 1;
+  const int total = s.tb.gtile[G] * args.n_tiles * csplit;
   const int kpb = args.K / BK;  // K blocks per pass over A
-  const int kblocks = kpb * args.ksplit;
+  const int kper = (kpb + csplit - 1) / csplit;  // K blocks of A per split
+  // the K blocks (in units of the ksplit-interleaved loop) of work unit `tile`; an output tile is
+  // tile / csplit, its split tile % csplit
+  auto krange = [&](int tile, int& k0, int& k1) {
+    const int sp = tile % csplit;
+    k0 = min(kpb, sp * kper) * args.ksplit;
+    k1 = min(kpb, (sp + 1) * kper) * args.ksplit;
+  };
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -139,7 +151,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     long long issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM, args.mode == 2);
+      Tile t = grp::decode(s.tb, G, args.n_tiles, tile / csplit, BM, args.mode == 2);
+      int kb0, kb1;
+      krange(tile, kb0, kb1);
       const CUtensorMap* mb = t.g < args.E ? &tmB : &tmBs;
       const int zg = t.g < args.E ? (args.slot_expert ? args.slot_expert[t.g] : t.g) : 0;
       int n0, n1;
@@ -153,7 +167,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         n0 = t.n_tile * BN;
         n1 = n0 + BN / 2;
       }
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_or_abort(&s.empty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
           break;
@@ -190,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // The accumulator holds one chunk of K blocks: the whole tile (modes 0, 1) or ROUTER_CHUNK
     // blocks (mode 2, whose epilogue adds the chunks in fp32).
     const uint32_t idesc = args.mode == 2 ? idesc_bf16(BM, BN / 2) : idesc_bf16(BM, BN);
-    const int ch_len = args.mode == 2 ? ROUTER_CHUNK : kblocks;
+    const int ch_len = args.mode == 2 ? ROUTER_CHUNK : kpb * args.ksplit;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -198,8 +212,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       uint32_t d = 0;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int kc = kb % ch_len;
+      int kb0, kb1;
+      krange(tile, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const int kc = (kb - kb0) % ch_len;
         if (kc == 0) {
           if (!wait_or_abort(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
             ok = false;
@@ -223,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           stage = 0;
           phase ^= 1;
         }
-        if (kc == ch_len - 1 || kb == kblocks - 1) {
+        if (kc == ch_len - 1 || kb == kb1 - 1) {
           umma_commit(&s.tfull[acc]);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1;
@@ -242,13 +258,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM, args.mode == 2);
+      Tile t = grp::decode(s.tb, G, args.n_tiles, tile / csplit, BM, args.mode == 2);
       if (args.mode == 2) {
         // router: sum the TMEM chunk partials of this tile in fp32 registers, then store
         float run[BN / 2];
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) run[i] = 0.f;
-        const int nch = (kblocks + ROUTER_CHUNK - 1) / ROUTER_CHUNK;
+        int kb0, kb1;
+        krange(tile, kb0, kb1);
+        const int nch = (kb1 - kb0 + ROUTER_CHUNK - 1) / ROUTER_CHUNK;
         bool fine = true;
         for (int ch = 0; ch < nch; ++ch) {
           int ok = 1;
@@ -278,7 +296,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!fine) break;
         const int ncols = min(BN / 2, args.n_valid - t.n_tile * (BN / 2));  // a multiple of 32
         if (r < t.rows) {
-          float* out = reinterpret_cast<float*>(args.out) + ((int64_t)t.a_row + r) * args.ldo + t.n_tile * (BN / 2);
+          float* out = reinterpret_cast<float*>(args.out) + (int64_t)(tile % csplit) * args.T * args.ldo +
+                       ((int64_t)t.a_row + r) * args.ldo + t.n_tile * (BN / 2);
 #pragma unroll
           for (int c = 0; c < BN / 2; c += 32)
             if (c < ncols) {
@@ -460,6 +479,7 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.I = d.I;
   a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, d.mode == 2 ? gg::BN / 2 : gg::BN);
   a.ksplit = ksplit;
+  a.csplit = d.mode == 2 && d.csplit > 1 ? d.csplit : 1;
   a.n_valid = d.N;
   a.ldo = d.ldo;
   a.out = d.out;
@@ -467,6 +487,24 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.status = d.status;
   a.wait_limit = 4000000000LL;  // about two seconds of SM clock
   gg::grouped_gemm_bf16_kernel<<<num_sms(), gg::THREADS, gg::SMEM_BYTES, stream>>>(tA, tB, tBs, a);
+  return cudaGetLastError();
+}
+
+// logits[i] = sum over s of partials[s][i], in split order (one thread per output element).
+__global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ partials, float* __restrict__ out,
+                                                            int splits, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    float v = partials[i];
+    for (int q = 1; q < splits; ++q) v = __fadd_rn(v, partials[(int64_t)q * n + i]);
+    out[i] = v;
+  }
+}
+
+cudaError_t launch_router_reduce(const float* partials, float* logits, int splits, int64_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = cdiv(n, 256);
+  if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
+  router_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(partials, logits, splits, n);
   return cudaGetLastError();
 }
 

@@ -77,12 +77,15 @@ struct GroupedGemmDesc {
   int E, R, T, K, N, I;
   int mode;  // 0 gate/up -> H, 1 down -> yd, 2 router logits (fp32)
   int ksplit = 1;  // mode 2: B holds 3 bf16 terms of the fp32 weight, [3, N, K]
+  int csplit = 1;  // mode 2: CTAs per output tile over disjoint K ranges; out = [csplit, T, ldo] partials
   void* out;
   int ldo;
   const float* row_weight;
   int* status;
 };
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
+// logits[i] = partials[0][i] + partials[1][i] + ... (split order), i < n
+cudaError_t launch_router_reduce(const float* partials, float* logits, int splits, int64_t n, cudaStream_t stream);
 // The expert FFN projections (modes 0 and 1) on CTA pairs: 256 x 256 tiles, tcgen05.mma.cta_group::2.
 cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
 
