@@ -69,9 +69,13 @@ __device__ __forceinline__ void build_table(Table& tb, const int32_t* offsets, i
   }
 }
 
-// Tile order: group-major, then output-column tile, then 128-row tile (so the CTAs running together
-// share one weight tile through L2); n_inner swaps the last two (the router: the activation rows are
-// the large operand).
+// Tile order: group-major; inside a group, bands of up to kBand row tiles, and inside a band the
+// output-column tile, then the row tile (so the CTAs running together share one weight tile through
+// L2, and a group with many rows -- the shared expert over a whole batch, a hot expert -- streams its
+// activation rows from DRAM once per band instead of once per column tile). A group of at most kBand
+// row tiles is one band. n_inner makes the column tile the innermost index (the router: the
+// activation rows are the large operand).
+constexpr int kBand = 8;
 __device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int tile, int BM, bool n_inner = false) {
   const int q = tile / n_tiles;
   int lo = 0, hi = G - 1;  // last g with gtile[g] <= q
@@ -90,8 +94,11 @@ __device__ __forceinline__ Tile decode(const Table& tb, int G, int n_tiles, int 
     t.m_tile = local / n_tiles;
     t.n_tile = local - t.m_tile * n_tiles;
   } else {
-    t.n_tile = local / mtc;
-    t.m_tile = local - t.n_tile * mtc;
+    const int band = local / (kBand * n_tiles);
+    const int rem = local - band * kBand * n_tiles;
+    const int bw = min(kBand, mtc - band * kBand);  // row tiles in this band
+    t.n_tile = rem / bw;
+    t.m_tile = band * kBand + (rem - t.n_tile * bw);
   }
   t.a_row = tb.grow[lo] + t.m_tile * BM;
   const int end = lo + 1 == tb.n_routed ? tb.gend : tb.grow[lo + 1];
