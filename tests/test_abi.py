@@ -82,6 +82,22 @@ def test_workspace_layout_is_ordered_and_aligned(lib):
         assert lay["total"] == moe.workspace_size(cfg)
 
 
+def test_scratch_holds_the_router_partial_sums_of_small_batches(lib):
+    """The tensor-core router (E >= 128) splits the K range of each 128 x 128 output tile over several
+    CTAs when a batch has fewer than 64 tiles; their fp32 partial sums live at the end of the scratch
+    region. A large batch needs none, so its scratch is the fixed part only."""
+    def scratch_bytes(T, E, h):
+        lay = moe.workspace_layout(_cfg(T=T, E=E, h=h, k=8, n_group=8, topk_group=4, score="sigmoid"))
+        return lay["total"] - lay["scratch"]
+
+    T, E, h = 256, 256, 7168  # decode: 2 x 2 tiles, 112 K blocks of 64 -> 28 splits of 4
+    big = scratch_bytes(16384, E, h)  # 128 x 2 tiles: no split
+    small = scratch_bytes(T, E, h)
+    assert small >= 28 * T * E * 4
+    assert small - 28 * T * E * 4 < big  # the rest is the status word and the histograms
+    assert scratch_bytes(T, 64, h) < 28 * T * 64 * 4  # E < 128: CUDA-core router, no partial sums
+
+
 def test_null_and_misaligned_pointers_are_rejected(lib):
     cfg = _cfg()
     w = moe.MoeWeightsStruct()
