@@ -55,6 +55,8 @@ SMALL = {
     "fp8_large_groups": _W["dsv3_fp8"].replace(name="fp8_large_groups", T=2200, h=512, E=8, k=4, n_group=2,
                                                topk_group=1, I=256, I_shared=256),
     "pair_cap": _W["mixtral"].replace(name="pair_cap", T=4500, h=256, I=256, capacity_factor=1.0),
+    # experts of more than 8 pair tiles (2250 rows): the tile order walks them in bands of 8 row tiles
+    "pair_bands": _W["mixtral"].replace(name="pair_bands", T=4500, h=256, E=4, I=256),
 }
 
 
