@@ -83,7 +83,8 @@ __device__ __forceinline__ uint32_t expand2(uint32_t byte, __half2 s2) {
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ,
+    grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
+                              const __grid_constant__ CUtensorMap tmQ,
                               const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmQs,
                               const __grid_constant__ CUtensorMap tmSs, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       s.abort_flag = 0;
       fence_mbar_init();
       tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA64);
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmS);
       tma_prefetch_desc(&tmQs);
@@ -142,6 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      const bool half = t.rows <= BM / 2;  // 64 rows or fewer: a 64-row activation box, an M = 64 MMA
       const bool routed = t.g < args.E;
       const CUtensorMap* mq = routed ? &tmQ : &tmQs;
       const CUtensorMap* ms = routed ? &tmS : &tmSs;
@@ -157,8 +160,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint8_t* a = ring_a + stage * A_BYTES;
         uint8_t* q = ring_q + stage * Q_BYTES;
-        mbar_arrive_expect_tx(&s.afull[stage], A_BYTES);
-        tma_load_2d(a, &tmA, &s.afull[stage], kb * BK, t.a_row);
+        mbar_arrive_expect_tx(&s.afull[stage], half ? A_BYTES / 2 : A_BYTES);
+        tma_load_2d(a, half ? &tmA64 : &tmA, &s.afull[stage], kb * BK, t.a_row);
         mbar_arrive_expect_tx(&s.qfull[stage], Q_BYTES);
         tma_load_3d(q, mq, &s.qfull[stage], kb * (BK / 2), r0, z);
         tma_load_3d(q + QC_BYTES / 2, mq, &s.qfull[stage], kb * (BK / 2), r1, z);
@@ -178,13 +181,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    const uint32_t idesc = idesc_bf16(BM, BN);
+    const uint32_t idesc_full = idesc_bf16(BM, BN), idesc_half = idesc_bf16(BM / 2, BN);
     int stage = 0, bst = 0;
     uint32_t phase = 0, bphase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const uint32_t idesc =
+          grp::decode(s.tb, G, args.n_tiles, tile, BM).rows <= BM / 2 ? idesc_half : idesc_full;
       if (!wait_or_abort(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) break;
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -273,18 +278,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global, times the matrix scale
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      // an M = 128 tile keeps row r in TMEM lane r; an M = 64 tile keeps rows 16q .. 16q + 15 in lanes
+      // 32q .. 32q + 15 (lanes 32q + 16 .. 32q + 31 hold nothing)
+      const bool half = t.rows <= BM / 2;
+      const int r = half ? quarter * 16 + (lane & 15) : quarter * 32 + lane;
       int ok = 1;
       if (lane == 0) ok = wait_or_abort(&s.tfull[acc], acc_phase, &s.abort_flag, args.status, args.wait_limit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
-      const bool valid = r < t.rows;
+      const bool valid = (!half || lane < 16) && r < t.rows;
       const int64_t orow = (int64_t)t.a_row + r;
       const float gs = t.g < args.E ? args.g[args.slot_expert ? args.slot_expert[t.g] : t.g] : args.g_shared[0];
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -433,8 +441,9 @@ cudaError_t launch_grouped_gemm_nvfp4(const GroupedGemmFp4Desc& d, cudaStream_t 
     attr_set = true;
   }
   const int64_t G = d.n_experts > 0 ? d.n_experts : d.E;
-  CUtensorMap tA, tQ, tS, tQs, tSs;
+  CUtensorMap tA, tA64, tQ, tS, tQs, tSs;
   bool ok = tma_encode_2d(&tA, d.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d.a_rows, d.K, g4::BM) &&
+            tma_encode_2d(&tA64, d.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d.a_rows, d.K, g4::BM / 2) &&
             tma_encode_3d_plain(&tQ, d.Bq, G, d.b_rows, d.K / 2, g4::BK / 2, g4::BN / 2) &&
             tma_encode_3d_plain(&tS, d.Bs, G, d.b_rows, d.K / 16, 16, g4::BN / 2) &&
             tma_encode_3d_plain(&tQs, d.Bq_shared ? d.Bq_shared : d.Bq, 1, d.b_rows, d.K / 2, g4::BK / 2, g4::BN / 2) &&
@@ -461,7 +470,7 @@ cudaError_t launch_grouped_gemm_nvfp4(const GroupedGemmFp4Desc& d, cudaStream_t 
   a.row_weight = d.row_weight;
   a.status = d.status;
   a.wait_limit = 4000000000LL;  // about two seconds of SM clock
-  g4::grouped_gemm_nvfp4_kernel<<<num_sms(), g4::THREADS, g4::SMEM_BYTES, stream>>>(tA, tQ, tS, tQs, tSs, a);
+  g4::grouped_gemm_nvfp4_kernel<<<num_sms(), g4::THREADS, g4::SMEM_BYTES, stream>>>(tA, tA64, tQ, tS, tQs, tSs, a);
   return cudaGetLastError();
 }
 
