@@ -304,6 +304,15 @@ int moe_eplb_plan(const int64_t* load, int32_t E, int32_t n_cards, int32_t n_red
  * MOE_ERR_CUDA. */
 int moe_device_status(const moe_config* cfg, void* ws, int32_t* status, moe_stream_t stream);
 
+/* Failure-detection self-test (no fault, no trap, no endless loop): one thread waits, through the
+ * bounded wait that every pipeline wait of the grouped GEMMs uses, on an mbarrier that nothing ever
+ * completes. After limit_cycles SM clocks (1 .. 4e9) the wait gives up and records
+ * MOE_STATUS_WAIT_TIMEOUT in the status word of ws, which moe_device_status then reports; the kernel
+ * returns and the context stays usable. Asynchronous on `stream`.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_WORKSPACE, MOE_ERR_CUDA. */
+int moe_selftest_wait_timeout(const moe_config* cfg, void* ws, size_t ws_bytes, int64_t limit_cycles,
+                              moe_stream_t stream);
+
 /* Message of the last non-zero status returned on the calling host thread ("" if none). */
 const char* moe_last_error(void);
 

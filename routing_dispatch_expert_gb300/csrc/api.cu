@@ -780,6 +780,19 @@ MOE_EXPORT int moe_eplb_plan(const int64_t* load, int32_t E, int32_t n_cards, in
   return MOE_OK;
 }
 
+MOE_EXPORT int moe_selftest_wait_timeout(const moe_config* cfg, void* ws, size_t ws_bytes, int64_t limit_cycles,
+                                         moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  Layout L = make_layout(cfg);
+  if ((rc = check_ws(ws, ws_bytes, L))) return rc;
+  if (limit_cycles < 1 || limit_cycles > 4000000000LL) return fail(MOE_ERR_INVALID, "limit_cycles must lie in [1, 4e9]");
+  cudaError_t e = moe::launch_wait_timeout_selftest(status_ptr(ws, L.l), (long long)limit_cycles, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  counted(1);
+  return MOE_OK;
+}
+
 MOE_EXPORT int moe_device_status(const moe_config* cfg, void* ws, int32_t* status, moe_stream_t stream) {
   int rc = check_config(cfg);
   if (rc) return rc;

@@ -490,6 +490,27 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   return cudaGetLastError();
 }
 
+// Failure-detection self-test: one thread waits, through the bounded wait every pipeline stage of
+// the grouped GEMMs uses, on an mbarrier that nothing arrives on. After `limit` SM clocks the wait
+// records MOE_STATUS_WAIT_TIMEOUT in *status and returns, so the kernel ends and the context stays
+// usable.
+__global__ void wait_timeout_selftest_kernel(int* status, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) grp::wait_or_abort(&bar, 0, &abort_flag, status, limit);  // phase 0 never completes
+}
+
+cudaError_t launch_wait_timeout_selftest(int* status, long long limit_cycles, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_cycles);
+  return cudaGetLastError();
+}
+
 // logits[i] = sum over s of partials[s][i], in split order (one thread per output element).
 __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ partials, float* __restrict__ out,
                                                             int splits, int64_t n) {

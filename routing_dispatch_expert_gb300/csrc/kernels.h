@@ -84,6 +84,8 @@ struct GroupedGemmDesc {
   int* status;
 };
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
+// one bounded mbarrier wait that nothing completes: records MOE_STATUS_WAIT_TIMEOUT in *status
+cudaError_t launch_wait_timeout_selftest(int* status, long long limit_cycles, cudaStream_t stream);
 // logits[i] = partials[0][i] + partials[1][i] + ... (split order), i < n
 cudaError_t launch_router_reduce(const float* partials, float* logits, int splits, int64_t n, cudaStream_t stream);
 // The expert FFN projections (modes 0 and 1) on CTA pairs: 256 x 256 tiles, tcgen05.mma.cta_group::2.

@@ -81,6 +81,7 @@ def load():
                 "moe_quantize_weights_fp8": [vp, i64, i64, i64, vp, vp, vp],
                 "moe_quantize_weights_nvfp4": [vp, i64, i64, i64, vp, vp, vp, vp],
                 "moe_device_status": [cfgp, vp, ctypes.POINTER(ctypes.c_int32), vp],
+                "moe_selftest_wait_timeout": [cfgp, vp, sz, i64, vp],
                 "moe_graph_create": [cfgp, vp, wp, vp, vp, sz, vp, ctypes.POINTER(vp)],
                 "moe_graph_launch": [vp, vp],
                 "moe_graph_destroy": [vp],
@@ -262,6 +263,13 @@ def device_status(cfg, ws) -> int:
     if rc not in (MOE_OK, MOE_ERR_DEVICE):
         _check(rc)
     return v.value
+
+
+def selftest_wait_timeout(cfg, ws, limit_cycles: int) -> None:
+    """Enqueue the failure-detection self-test (moe_selftest_wait_timeout): a bounded wait that nothing
+    completes records MOE_STATUS_WAIT_TIMEOUT in the workspace's status word."""
+    _check(load().moe_selftest_wait_timeout(ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                                            int(limit_cycles), _stream()))
 
 
 def balance(cfg, ws) -> dict:

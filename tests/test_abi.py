@@ -98,6 +98,15 @@ def test_scratch_holds_the_router_partial_sums_of_small_batches(lib):
     assert scratch_bytes(T, 64, h) < 28 * T * 64 * 4  # E < 128: CUDA-core router, no partial sums
 
 
+def test_wait_timeout_selftest_checks_its_arguments(lib):
+    """The failure-detection self-test rejects a limit outside [1, 4e9] before any CUDA call."""
+    cfg = _cfg()
+    fake_ws = ctypes.c_void_p(1 << 20)  # never dereferenced: the call fails on the limit first
+    big = ctypes.c_size_t(1 << 40)
+    for bad in (0, -5, 5_000_000_000):
+        assert lib.moe_selftest_wait_timeout(ctypes.byref(cfg), fake_ws, big, bad, None) == moe.MOE_ERR_INVALID
+
+
 def test_null_and_misaligned_pointers_are_rejected(lib):
     cfg = _cfg()
     w = moe.MoeWeightsStruct()

@@ -272,6 +272,23 @@ def test_bad_expert_index_is_skipped_and_reported():
     assert sorted(rows.tolist()) == list(range(int(valid.sum())))
 
 
+def test_timed_out_wait_is_reported_and_the_context_survives():
+    """Failure detection without a fault: a bounded mbarrier wait that nothing completes gives up after
+    its limit, records MOE_STATUS_WAIT_TIMEOUT, and the next layer call on the same GPU is correct."""
+    wl = SMALL["dsv3_small"]
+    L = GpuLayer(wl)
+    rde.device_status(L.cfg, L.ws)  # clear
+    rde.selftest_wait_timeout(L.cfg, L.ws, 2_000_000)  # about a millisecond of SM clock
+    torch.cuda.synchronize()
+    assert rde.device_status(L.cfg, L.ws) == rde.moe.MOE_STATUS_WAIT_TIMEOUT
+    assert rde.device_status(L.cfg, L.ws) == 0  # read and cleared
+    y = L.forward()
+    assert rde.device_status(L.cfg, L.ws) == 0
+    ref = oracle.bf16_to_double(bits(y))
+    assert np.isfinite(ref).all()
+    _check_layer_against_oracle(wl, L)
+
+
 def test_fp8_dispatch_is_bit_exact():
     wl = SMALL["dsv3_small"].replace(dtype="fp8")
     cfg = cfg_of(wl)
