@@ -13,7 +13,9 @@
 //           three bf16 terms [3, E, h]; x is exact in bf16 and every bf16 x bf16 product is exact in
 //           fp32. The tensor core's accumulator does not round like an IEEE fp32 add over thousands
 //           of steps, so the MMAs accumulate chunks of ROUTER_CHUNK K blocks in TMEM (double
-//           buffered, 128-column tiles) and the epilogue sums the chunks in fp32 registers. A batch
+//           buffered) and the epilogue sums the chunks in fp32 registers. The router runs a
+//           320-thread instantiation: 256-column tiles drained by eight epilogue warps (two per
+//           TMEM lane quarter), or 128-column tiles by four when the K range is split. A batch
 //           too small to fill the SMs splits each tile's K range over `csplit` CTAs, which write fp32
 //           partial sums that launch_router_reduce adds in split order.
 // Work follows the device-side per-expert counts (Perplexity, "Quantization": kernels read the
@@ -52,7 +54,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;          // warps 0 TMA, 1 MMA, 2-5 epilogue
+constexpr int ROUTER_THREADS = 320;   // the router's instantiation: warps 2-9 drain 256-column tiles
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr int ROUTER_CHUNK = 8;  // K blocks (512 K elements) per TMEM partial sum in mode 2
@@ -72,6 +75,7 @@ struct Args {
   int csplit;   // mode 2: CTAs sharing one output tile, each over a contiguous range of K (1: none);
                 // split s writes its fp32 partial sums to out + s * T * ldo
   int n_valid;  // mode 2: output columns that exist (E)
+  int rbn;      // mode 2: output tile width, 128 or 256 (256 needs the ROUTER_THREADS instantiation)
   int ldo;      // output row stride in elements
   void* out;
   const float* row_weight;
@@ -94,7 +98,8 @@ using grp::silu;
 using grp::Tile;
 using grp::wait_or_abort;
 
-__global__ void __launch_bounds__(THREADS, 1)
+template <int NT>
+__global__ void __launch_bounds__(NT, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmBs, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 4);
+        mbar_init(&s.tempty[i], args.mode == 2 && args.rbn == BN ? 8 : 4);
       }
       mbar_init(&s.mma_done, 1);
       s.abort_flag = 0;
@@ -161,8 +166,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         n0 = t.n_tile * (BN / 2);
         n1 = args.I + t.n_tile * (BN / 2);
       } else if (args.mode == 2) {
-        n0 = t.n_tile * (BN / 2);  // 128-wide tiles: one B box
-        n1 = -1;
+        n0 = t.n_tile * args.rbn;  // 128-wide tiles: one B box; 256-wide: two (rows past E read as zero)
+        n1 = args.rbn == BN ? n0 + BN / 2 : -1;
       } else {
         n0 = t.n_tile * BN;
         n1 = n0 + BN / 2;
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- MMA issuer
     // The accumulator holds one chunk of K blocks: the whole tile (modes 0, 1) or ROUTER_CHUNK
     // blocks (mode 2, whose epilogue adds the chunks in fp32).
-    const uint32_t idesc = args.mode == 2 ? idesc_bf16(BM, BN / 2) : idesc_bf16(BM, BN);
+    const uint32_t idesc = args.mode == 2 ? idesc_bf16(BM, args.rbn) : idesc_bf16(BM, BN);
     const int ch_len = args.mode == 2 ? ROUTER_CHUNK : kpb * args.ksplit;
     int stage = 0;
     uint32_t phase = 0;
@@ -251,9 +256,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     long long t0 = clock64();
     while (!mbar_try_wait(&s.mma_done, 0) && clock64() - t0 < args.wait_limit) {
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && (warp < 6 || (args.mode == 2 && args.rbn == BN))) {
     // ---------------- epilogue: TMEM -> registers -> global
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32)
+    const int chalf = (warp - 2) >> 2;  // mode 2 with 256-wide tiles: which 128 of the tile's columns
     const int r = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -278,7 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           __syncwarp();
           tc_fence_after();
-          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+          const uint32_t taddr =
+              tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + chalf * (BN / 2));
 #pragma unroll
           for (int c = 0; c < BN / 2; c += 32) {
             uint32_t v[32];
@@ -294,10 +301,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (acc == 0) acc_phase ^= 1;
         }
         if (!fine) break;
-        const int ncols = min(BN / 2, args.n_valid - t.n_tile * (BN / 2));  // a multiple of 32
+        const int col0 = t.n_tile * args.rbn + chalf * (BN / 2);
+        const int ncols = min(BN / 2, args.n_valid - col0);  // a multiple of 32 (may be <= 0)
         if (r < t.rows) {
           float* out = reinterpret_cast<float*>(args.out) + (int64_t)(tile % csplit) * args.T * args.ldo +
-                       ((int64_t)t.a_row + r) * args.ldo + t.n_tile * (BN / 2);
+                       ((int64_t)t.a_row + r) * args.ldo + col0;
 #pragma unroll
           for (int c = 0; c < BN / 2; c += 32)
             if (c < ncols) {
@@ -448,8 +456,11 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   }
   static bool attr_set = false;
   if (!attr_set) {
-    e = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel<gg::THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gg::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel<gg::ROUTER_THREADS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
     if (e != cudaSuccess) {
       *err = "cudaFuncSetAttribute failed";
       return e;
@@ -477,7 +488,10 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.mode = d.mode;
   a.slot_expert = d.slot_expert;
   a.I = d.I;
-  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, d.mode == 2 ? gg::BN / 2 : gg::BN);
+  // the router: 256-wide tiles (one pass over each activation tile for 256 experts) unless its K range is
+  // split over CTAs (a small batch), where 128-wide tiles keep the partial sums small
+  a.rbn = d.mode == 2 && d.csplit <= 1 ? gg::BN : gg::BN / 2;
+  a.n_tiles = d.mode == 0 ? d.I / (gg::BN / 2) : (int)cdiv(d.N, d.mode == 2 ? a.rbn : gg::BN);
   a.ksplit = ksplit;
   a.csplit = d.mode == 2 && d.csplit > 1 ? d.csplit : 1;
   a.n_valid = d.N;
@@ -486,7 +500,11 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.row_weight = d.row_weight;
   a.status = d.status;
   a.wait_limit = 4000000000LL;  // about two seconds of SM clock
-  gg::grouped_gemm_bf16_kernel<<<num_sms(), gg::THREADS, gg::SMEM_BYTES, stream>>>(tA, tB, tBs, a);
+  if (d.mode == 2)
+    gg::grouped_gemm_bf16_kernel<gg::ROUTER_THREADS>
+        <<<num_sms(), gg::ROUTER_THREADS, gg::SMEM_BYTES, stream>>>(tA, tB, tBs, a);
+  else
+    gg::grouped_gemm_bf16_kernel<gg::THREADS><<<num_sms(), gg::THREADS, gg::SMEM_BYTES, stream>>>(tA, tB, tBs, a);
   return cudaGetLastError();
 }
 
