@@ -143,8 +143,9 @@ typedef struct {
   size_t h_scales;   /* FP8: [R_tot, I/128] fp32 */
   size_t yd;         /* [R_tot, h] bf16 expert outputs (routed rows already route-weighted) */
   size_t router_w3;  /* [3, E, h] bf16: the router weight as three bf16 terms (tensor-core router) */
-  size_t scratch;    /* per-call scratch (status word, histograms; for a batch too small to fill the
-                        SMs with router tiles, the router's fp32 partial sums) */
+  size_t scratch;    /* per-call scratch (status word, the grouped GEMMs' tile counters, histograms;
+                        for a batch too small to fill the SMs with router tiles, the router's fp32
+                        partial sums) */
   size_t total;      /* bytes required */
 } moe_ws_layout;
 

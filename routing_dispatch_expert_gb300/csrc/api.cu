@@ -129,6 +129,13 @@ Layout make_layout(const moe_config* c) {
 int* status_ptr(void* ws, const moe_ws_layout& l) {
   return reinterpret_cast<int*>(static_cast<char*>(ws) + l.scratch);
 }
+// tile counters of the CTA-pair grouped GEMM launches, in the scratch header after the status word:
+// [0] gate/up and [1] down of the routed launches, [2] and [3] those of the shared expert's launches
+// on the second stream. moe_forward zeroes them with the status word; moe_expert_ffn zeroes the
+// routed pair on its own stream.
+constexpr int kTileCounters = 4;
+static_assert((16 + kTileCounters) * sizeof(int) <= 256, "the scratch header holds the status word and the tile counters");
+int* tile_ctr_ptr(void* ws, const moe_ws_layout& l) { return status_ptr(ws, l) + 16; }
 int32_t* hist_ptr(void* ws, const moe_ws_layout& l) {
   return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + l.scratch + 256);
 }
@@ -282,7 +289,7 @@ bool use_pair_tiles(const moe_config* c, int S) {
 
 int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, const float* xd_scales,
                   const int32_t* offsets, const float* row_weight, void* yd, void* ws, const Layout& L,
-                  cudaStream_t stream, bool with_shared = true) {
+                  cudaStream_t stream, bool with_shared = true, bool reset_ctr = true) {
   if (c->T == 0) return MOE_OK;
   const bool shared = c->I_shared > 0 && with_shared;
   std::string err;
@@ -381,7 +388,13 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
     counted(2);
     return MOE_OK;
   }
-  auto launch = use_pair_tiles(c, S) ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
+  const bool pairs = use_pair_tiles(c, S);
+  auto launch = pairs ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
+  int* ctr = tile_ctr_ptr(ws, L.l);
+  if (pairs && reset_ctr) {
+    cudaError_t e = cudaMemsetAsync(ctr, 0, 2 * sizeof(int), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tile counter reset");
+  }
   moe::GroupedGemmDesc g;
   g.slot_expert = slot_expert;
   g.n_experts = c->E;
@@ -402,6 +415,7 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
   g.ldo = c->I;
   g.row_weight = nullptr;
   g.status = status_ptr(ws, L.l);
+  g.tile_ctr = pairs ? ctr : nullptr;
   cudaError_t e = launch(g, stream, &err);
   if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "gate/up grouped GEMM launch") : cuda_fail(e, err.c_str());
   g.A = at<void>(ws, L.l.hbuf);
@@ -414,6 +428,7 @@ int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, con
   g.out = yd;
   g.ldo = c->h;
   g.row_weight = row_weight;
+  g.tile_ctr = pairs ? ctr + 1 : nullptr;
   e = launch(g, stream, &err);
   if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "down grouped GEMM launch") : cuda_fail(e, err.c_str());
   counted(2);
@@ -431,7 +446,9 @@ int do_shared_ffn_bf16(const moe_config* c, const moe_weights* w, const void* x,
   std::string err;
   // the kernel the shared group would get inside the routed launch, so that both paths compute its
   // rows with the same tiles (bit-identical outputs)
-  auto launch = use_pair_tiles(c, (int)n_groups(c)) ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
+  const bool pairs = use_pair_tiles(c, (int)n_groups(c));
+  auto launch = pairs ? moe::launch_grouped_gemm_bf16_pair : moe::launch_grouped_gemm_bf16;
+  int* ctr = tile_ctr_ptr(ws, L.l) + 2;  // zeroed by moe_forward, the only caller
   __nv_bfloat16* hs = at<__nv_bfloat16>(ws, L.l.hbuf) + L.R * (int64_t)c->I;
   __nv_bfloat16* ys = at<__nv_bfloat16>(ws, L.l.yd) + L.R * (int64_t)c->h;
   moe::GroupedGemmDesc g;
@@ -454,6 +471,7 @@ int do_shared_ffn_bf16(const moe_config* c, const moe_weights* w, const void* x,
   g.ldo = c->I;
   g.row_weight = nullptr;
   g.status = status_ptr(ws, L.l);
+  g.tile_ctr = pairs ? ctr : nullptr;
   cudaError_t e = launch(g, stream, &err);
   if (e != cudaSuccess)
     return err.empty() ? cuda_fail(e, "shared-expert gate/up launch") : cuda_fail(e, err.c_str());
@@ -466,6 +484,7 @@ int do_shared_ffn_bf16(const moe_config* c, const moe_weights* w, const void* x,
   g.mode = 1;
   g.out = ys;
   g.ldo = c->h;
+  g.tile_ctr = pairs ? ctr + 1 : nullptr;
   e = launch(g, stream, &err);
   if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "shared-expert down launch") : cuda_fail(e, err.c_str());
   counted(2);
@@ -636,7 +655,8 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   REQUIRE_PTR(weights->w_router, "weights->w_router");
   if ((rc = check_expert_weights(cfg, weights))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(status_ptr(ws, L.l), 0, sizeof(int), s);
+  // the status word and the grouped GEMMs' tile counters
+  cudaError_t e = cudaMemsetAsync(status_ptr(ws, L.l), 0, (16 + kTileCounters) * sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
   const moe_ws_layout& l = L.l;
   if ((rc = do_route(cfg, x, weights, at<float>(ws, l.logits), 0, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w),
@@ -668,7 +688,7 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
     return rc;
   }
   if ((rc = do_expert_ffn(cfg, weights, at<void>(ws, l.xd), at<float>(ws, l.xd_scales), at<int32_t>(ws, l.offsets),
-                          at<float>(ws, l.row_weight), at<void>(ws, l.yd), ws, L, s, !side))) {
+                          at<float>(ws, l.row_weight), at<void>(ws, l.yd), ws, L, s, !side, false))) {
     if (side) cudaStreamWaitEvent(s, sd->join, 0);
     return rc;
   }

@@ -110,11 +110,17 @@ constexpr uint32_t kWaitSleepNs = 20000;  // one suspension of a waiting thread:
 
 // Bounded wait on an mbarrier phase. Gives up when another role of the CTA has aborted, or after
 // `limit` SM clocks (then it raises the CTA's abort flag and records MOE_STATUS_WAIT_TIMEOUT).
+// With kCluster the wait acquires at cluster scope (a phase completed from the other CTA of a pair).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                               long long limit) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() {
+    return kCluster ? mbar_try_wait_sleep_cluster(bar, parity, kWaitSleepNs)
+                    : mbar_try_wait_sleep(bar, parity, kWaitSleepNs);
+  };
+  if (!kCluster && mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
+  while (!poll()) {
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;

@@ -21,9 +21,18 @@
 // interleaved (leader: gate 0-63 and up 0-63 of the column tile; follower: gate 64-127 and up
 // 64-127), so each lane still holds the gate and up value of its outputs.
 //
+// Schedule: persistent pairs take tiles in index order from a tile counter in global memory (one
+// atomic per tile). Every pair starts on tile `pair`; the next tile is the counter's value plus the
+// number of pairs. Pairs that run at the same time thus hold neighbouring tiles, which share a weight
+// tile (row tiles of one column tile are neighbours) or a row tile, however unequal the tiles are
+// (half tiles, short groups); a fixed stride per pair lets the pairs drift apart, after which those
+// tiles are read from DRAM again. Without a counter the pair walks tiles pair, pair + pairs, ...
+//
 // Roles (192 threads per CTA; CTA rank 0 of the cluster is the leader):
 //   * warp 0 lane 0 of each CTA: TMA producer into its own 6-stage ring; completions are counted on
-//     the leader's `full` barrier (the leader posts the expected bytes of both CTAs);
+//     the leader's `full` barrier (the leader posts the expected bytes of both CTAs). The leader's
+//     producer is also the scheduler: it takes the next tile from the counter and posts it in a ring
+//     of slots in both CTAs (`tnext`), which the other roles read and release (`tfree`);
 //   * warp 1 lane 0 of the leader: issues the pair MMAs (M 256, N 256, K 16) into the accumulator
 //     (TMEM, 2 x 256 columns in each CTA, double buffered) and commits to both CTAs' `empty` and
 //     `tfull` barriers at once (multicast);
@@ -55,6 +64,8 @@ constexpr int B_BYTES = BNH * BK * 2;   // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
+constexpr int TRING = 4;                // schedule slots (tile indices handed from the scheduler to the roles)
+constexpr int TREADERS = 10;            // readers of a slot: leader MMA + 4 epilogue warps, follower producer + 4
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 
 struct Args {
@@ -64,6 +75,7 @@ struct Args {
   void* out;
   const float* row_weight;
   int* status;
+  int* tile_ctr;  // tile counter (zero before the launch), or nullptr: fixed stride
   long long wait_limit;
 };
 
@@ -73,6 +85,9 @@ struct Shared {
   uint64_t tfull[2];        // each CTA: accumulator buffer complete
   uint64_t tempty[2];       // leader only: both CTAs drained the accumulator buffer
   uint64_t mma_done;
+  uint64_t tnext[TRING];    // each CTA: the slot holds the next tile (the leader's scheduler arrives)
+  uint64_t tfree[TRING];    // leader only: every reader of the slot has taken the tile
+  int next_tile[TRING];
   uint32_t tmem_slot;
   volatile int abort_flag;
   grp::Table tb;
@@ -107,6 +122,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(&s.tempty[i], 8);
       }
       mbar_init(&s.mma_done, 1);
+      for (int i = 0; i < TRING; ++i) {
+        mbar_init(&s.tnext[i], 1);
+        mbar_init(&s.tfree[i], TREADERS);
+      }
       s.abort_flag = 0;
       fence_mbar_init();
       tma_prefetch_desc(&tmA);
@@ -127,6 +146,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = s.tmem_slot;
   const int total = s.tb.gtile[G] * args.n_tiles;
   const int kblocks = args.K / BK;
+  const uint32_t tfree0 = mapa_shared(smem_u32(&s.tfree[0]), 0);  // the leader's tfree[0]
+  // the tile in schedule slot `it` (a reader other than the scheduler): wait for it, take it, release
+  // the slot; -1 when the wait gave up
+  auto take_tile = [&](int it) -> int {
+    const int slot = it % TRING;
+    if (!wait_or_abort<true>(&s.tnext[slot], (uint32_t)((it / TRING) & 1), &s.abort_flag, args.status,
+                             args.wait_limit))
+      return -1;
+    const int t = *reinterpret_cast<volatile int*>(&s.next_tile[slot]);
+    mbar_arrive_cluster(tfree0 + (uint32_t)(slot * sizeof(uint64_t)));
+    return t;
+  };
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer (both CTAs)
@@ -135,7 +166,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     long long issued = 0;
     bool ok = true;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
+    const uint32_t peer_next0 = mapa_shared(smem_u32(&s.next_tile[0]), 1);
+    const uint32_t peer_tnext0 = mapa_shared(smem_u32(&s.tnext[0]), 1);
+    int tile = pair;
+    for (int it = 0; ok; ++it) {
+      if (rank == 0) {
+        // scheduler: post `tile` in slot `it` of both CTAs once every reader has released its last use
+        const int slot = it % TRING;
+        if (!wait_or_abort<true>(&s.tfree[slot], (uint32_t)(((it / TRING) & 1) ^ 1), &s.abort_flag, args.status,
+                                 args.wait_limit))
+          break;
+        st_shared_cluster_u32(peer_next0 + (uint32_t)(slot * sizeof(int)), (uint32_t)tile);
+        mbar_arrive_cluster(peer_tnext0 + (uint32_t)(slot * sizeof(uint64_t)));
+        *reinterpret_cast<volatile int*>(&s.next_tile[slot]) = tile;
+        mbar_arrive(&s.tnext[slot]);
+      } else {
+        tile = take_tile(it);
+        if (tile < 0) break;
+      }
+      if (tile >= total) break;
+      // the leader takes the following tile now; the atomic's latency hides behind this tile's copies
+      const int next = rank == 0 ? (args.tile_ctr ? npairs + atomicAdd(args.tile_ctr, 1) : tile + npairs) : 0;
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, PM);
       const bool half = t.rows <= BM;  // the M = 128 pair tile: 64 rows per CTA
       const bool gu_half = half && args.mode == 0;
@@ -168,6 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           phase ^= 1;
         }
       }
+      tile = next;
     }
     // the leader's last fills of every stage (both CTAs' bytes) must land before either CTA exits;
     // the follower is held by the final cluster barrier until the leader has seen them
@@ -184,7 +236,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
+    for (int it = 0; ok; ++it) {
+      const int tile = take_tile(it);
+      if (tile < 0 || tile >= total) break;
       const uint32_t idesc = grp::decode(s.tb, G, args.n_tiles, tile, PM).rows <= BM ? idesc_half : idesc_full;
       if (!wait_or_abort(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) break;
       tc_fence_after();
@@ -220,7 +274,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);  // the leader's tempty[0]
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < total; tile += npairs) {
+    for (int it = 0;; ++it) {
+      int tile = 0;
+      if (lane == 0) tile = take_tile(it);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile < 0 || tile >= total) break;
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, PM);
       int ok = 1;
       if (lane == 0) ok = wait_or_abort(&s.tfull[acc], acc_phase, &s.abort_flag, args.status, args.wait_limit);
@@ -368,6 +426,7 @@ cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t
   a.out = d.out;
   a.row_weight = d.row_weight;
   a.status = d.status;
+  a.tile_ctr = d.tile_ctr;
   a.wait_limit = 4000000000LL;  // about two seconds of SM clock
   cfg.gridDim = dim3(2 * max_pairs);
   e = cudaLaunchKernelEx(&cfg, g2::grouped_gemm_bf16_pair_kernel, tA, tB, tBs, tB64, tBs64, a);

@@ -82,6 +82,9 @@ struct GroupedGemmDesc {
   int ldo;
   const float* row_weight;
   int* status;
+  // CTA-pair kernel: a zeroed int from which the persistent pairs take tiles in index order
+  // (nullptr: each pair walks a fixed stride). The single-CTA kernel ignores it.
+  int* tile_ctr = nullptr;
 };
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
 // one bounded mbarrier wait that nothing completes: records MOE_STATUS_WAIT_TIMEOUT in *status
