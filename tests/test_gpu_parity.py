@@ -55,6 +55,9 @@ SMALL = {
     "fp8_large_groups": _W["dsv3_fp8"].replace(name="fp8_large_groups", T=2200, h=512, E=8, k=4, n_group=2,
                                                topk_group=1, I=256, I_shared=256),
     "pair_cap": _W["mixtral"].replace(name="pair_cap", T=4500, h=256, I=256, capacity_factor=1.0),
+    # pairs with a shared expert and dropped slots
+    "pair_cap_shared": _W["dsv3_prefill"].replace(name="pair_cap_shared", T=1500, h=256, E=8, k=4, n_group=2,
+                                                  topk_group=1, I=256, I_shared=256, capacity_factor=1.0),
     # experts of more than 8 pair tiles (2250 rows): the tile order walks them in bands of 8 row tiles
     "pair_bands": _W["mixtral"].replace(name="pair_bands", T=4500, h=256, E=4, I=256),
 }
@@ -152,8 +155,10 @@ def test_forward_matches_oracle(name):
     _check_layer_against_oracle(wl, L, min_clear=0.0 if name == "dsv3_hot" else 0.5)
 
 
-def test_forward_is_deterministic():
-    wl = SMALL["dsv3_small"]
+# dsv3_small: single-CTA tiles; pair_dsv3: CTA pairs (both with the shared expert on the second stream)
+@pytest.mark.parametrize("name", ["dsv3_small", "pair_dsv3"])
+def test_forward_is_deterministic(name):
+    wl = SMALL[name]
     L = GpuLayer(wl)
     y1 = L.forward().clone()
     yd1 = L.intermediates()["yd"].clone()
@@ -162,10 +167,11 @@ def test_forward_is_deterministic():
     assert torch.equal(yd1.view(torch.int16), L.intermediates()["yd"].view(torch.int16))
 
 
-def test_steps_through_their_own_entry_points():
+@pytest.mark.parametrize("name", ["dsv3_small", "pair_dsv3"])
+def test_steps_through_their_own_entry_points(name):
     """moe_route (with and without given logits), moe_dispatch, moe_expert_ffn and moe_combine called
     one by one give what moe_forward gives."""
-    wl = SMALL["dsv3_small"]
+    wl = SMALL[name]
     L = GpuLayer(wl)
     y_fwd = L.forward().clone()
     it = L.intermediates()
