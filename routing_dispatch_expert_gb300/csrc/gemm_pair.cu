@@ -31,8 +31,9 @@
 // Roles (192 threads per CTA; CTA rank 0 of the cluster is the leader):
 //   * warp 0 lane 0 of each CTA: TMA producer into its own 6-stage ring; completions are counted on
 //     the leader's `full` barrier (the leader posts the expected bytes of both CTAs). The leader's
-//     producer is also the scheduler: it takes the next tile from the counter and posts it in a ring
-//     of slots in both CTAs (`tnext`), which the other roles read and release (`tfree`);
+//     producer is also the scheduler: it takes the tiles from the counter and posts each one, a
+//     tile ahead, in a ring of slots in both CTAs (`tnext`), which the other roles read and release
+//     (`tfree`);
 //   * warp 1 lane 0 of the leader: issues the pair MMAs (M 256, N 256, K 16) into the accumulator
 //     (TMEM, 2 x 256 columns in each CTA, double buffered) and commits to both CTAs' `empty` and
 //     `tfull` barriers at once (multicast);
@@ -168,25 +169,38 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     const uint32_t peer_next0 = mapa_shared(smem_u32(&s.next_tile[0]), 1);
     const uint32_t peer_tnext0 = mapa_shared(smem_u32(&s.tnext[0]), 1);
-    int tile = pair;
+    // scheduler (leader): post tile `t` in slot `j` of both CTAs once every reader has released the
+    // slot's previous tile (false when that wait gave up); take the tile that follows `t`
+    auto post = [&](int j, int t) -> bool {
+      const int slot = j % TRING;
+      if (!wait_or_abort<true>(&s.tfree[slot], (uint32_t)(((j / TRING) & 1) ^ 1), &s.abort_flag, args.status,
+                               args.wait_limit))
+        return false;
+      st_shared_cluster_u32(peer_next0 + (uint32_t)(slot * sizeof(int)), (uint32_t)t);
+      mbar_arrive_cluster(peer_tnext0 + (uint32_t)(slot * sizeof(uint64_t)));
+      *reinterpret_cast<volatile int*>(&s.next_tile[slot]) = t;
+      mbar_arrive(&s.tnext[slot]);
+      return true;
+    };
+    auto fetch = [&](int t) -> int { return args.tile_ctr ? npairs + atomicAdd(args.tile_ctr, 1) : t + npairs; };
+    // The leader posts each tile one whole tile ahead of its copies, so that no reader (the follower's
+    // copies above all) waits for it at a tile boundary, and takes the tile after it at the same time
+    // (the atomic's latency hides behind a tile's copies).
+    int tile = pair, next = 0;
+    if (rank == 0) {
+      ok = post(0, tile);
+      next = tile < total ? fetch(tile) : tile;
+    }
     for (int it = 0; ok; ++it) {
+      int after = 0;  // leader: the tile after `next`
       if (rank == 0) {
-        // scheduler: post `tile` in slot `it` of both CTAs once every reader has released its last use
-        const int slot = it % TRING;
-        if (!wait_or_abort<true>(&s.tfree[slot], (uint32_t)(((it / TRING) & 1) ^ 1), &s.abort_flag, args.status,
-                                 args.wait_limit))
-          break;
-        st_shared_cluster_u32(peer_next0 + (uint32_t)(slot * sizeof(int)), (uint32_t)tile);
-        mbar_arrive_cluster(peer_tnext0 + (uint32_t)(slot * sizeof(uint64_t)));
-        *reinterpret_cast<volatile int*>(&s.next_tile[slot]) = tile;
-        mbar_arrive(&s.tnext[slot]);
+        if (tile >= total) break;
+        if (!post(it + 1, next)) break;
+        after = next < total ? fetch(next) : next;
       } else {
         tile = take_tile(it);
-        if (tile < 0) break;
+        if (tile < 0 || tile >= total) break;
       }
-      if (tile >= total) break;
-      // the leader takes the following tile now; the atomic's latency hides behind this tile's copies
-      const int next = rank == 0 ? (args.tile_ctr ? npairs + atomicAdd(args.tile_ctr, 1) : tile + npairs) : 0;
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, PM);
       const bool half = t.rows <= BM;  // the M = 128 pair tile: 64 rows per CTA
       const bool gu_half = half && args.mode == 0;
@@ -219,7 +233,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           phase ^= 1;
         }
       }
-      tile = next;
+      if (rank == 0) {
+        tile = next;
+        next = after;
+      }
     }
     // the leader's last fills of every stage (both CTAs' bytes) must land before either CTA exits;
     // the follower is held by the final cluster barrier until the leader has seen them
