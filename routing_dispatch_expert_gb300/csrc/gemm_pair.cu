@@ -150,13 +150,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tfree0 = mapa_shared(smem_u32(&s.tfree[0]), 0);  // the leader's tfree[0]
   // the tile in schedule slot `it` (a reader other than the scheduler): wait for it, take it, release
   // the slot; -1 when the wait gave up
+  // The leader's readers wait and arrive at CTA scope (the scheduler is a thread of their own CTA);
+  // only the follower's readers need cluster scope.
   auto take_tile = [&](int it) -> int {
     const int slot = it % TRING;
-    if (!wait_or_abort<true>(&s.tnext[slot], (uint32_t)((it / TRING) & 1), &s.abort_flag, args.status,
-                             args.wait_limit))
-      return -1;
+    const uint32_t par = (uint32_t)((it / TRING) & 1);
+    const bool got = rank == 0
+                         ? wait_or_abort(&s.tnext[slot], par, &s.abort_flag, args.status, args.wait_limit)
+                         : wait_or_abort<true>(&s.tnext[slot], par, &s.abort_flag, args.status, args.wait_limit);
+    if (!got) return -1;
     const int t = *reinterpret_cast<volatile int*>(&s.next_tile[slot]);
-    mbar_arrive_cluster(tfree0 + (uint32_t)(slot * sizeof(uint64_t)));
+    if (rank == 0)
+      mbar_arrive(&s.tfree[slot]);
+    else
+      mbar_arrive_cluster(tfree0 + (uint32_t)(slot * sizeof(uint64_t)));
     return t;
   };
 
