@@ -514,6 +514,7 @@ def main():
         raise SystemExit(f"device status {status} after the timed region")
 
     peaks, peaks_kind = load_peaks()
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flops, gemm_flops, bytes_ = layer_counts(wl, active)
     p_tc = peaks["bf16_tflops"] * 1e12
     p_hbm = peaks["hbm_gbs"] * 1e9
@@ -532,7 +533,7 @@ def main():
         gemm_kernel = "grouped_gemm_fp8_kernel"
     elif wl.dtype == "nvfp4":
         gemm_kernel = "grouped_gemm_nvfp4_kernel"
-    elif wl.T * wl.k >= 128 * wl.E:
+    elif wl.T * wl.k >= 128 * wl.E and (wl.T * wl.k // 256) * (wl.I // 128) > n_sms // 2:
         gemm_kernel = "grouped_gemm_bf16_pair_kernel"
     else:
         gemm_kernel = "grouped_gemm_bf16_kernel"

@@ -281,10 +281,14 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
 // tile) move less shared memory per MMA than single-CTA tiles, but each CTA stages only half a weight
 // tile per K step: a weight-streaming step (a few rows per expert) keeps more weight bytes in flight on
 // single CTAs. (The FP8 kernel stays on single CTAs: its per-K-block promotion hand-off would have to
-// cross the pair every 128 K elements.)
+// cross the pair every 128 K elements.) A layer whose full pair tiles of the gate/up launch would not
+// exceed one wave of pairs (the tiny layer: 64 tiles for 76 pairs) also stays on single CTAs: twice
+// as many tiles for the same SMs, so no pair runs a second tile while the others idle.
 constexpr int64_t kPairMinRowsPerGroup = 128;
 bool use_pair_tiles(const moe_config* c, int S) {
-  return S > 0 && (int64_t)c->T * c->k >= kPairMinRowsPerGroup * S;
+  if (S <= 0 || (int64_t)c->T * c->k < kPairMinRowsPerGroup * S) return false;
+  const int64_t pair_tiles = ((int64_t)c->T * c->k / 256) * (c->I / 128);
+  return pair_tiles > moe::num_sms() / 2;
 }
 
 int do_expert_ffn(const moe_config* c, const moe_weights* w, const void* xd, const float* xd_scales,

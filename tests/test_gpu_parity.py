@@ -45,21 +45,21 @@ SMALL = {
     "fp4_large_groups": _W["dsv3_decode_fp4"].replace(name="fp4_large_groups", T=2200, h=512, E=8, k=4,
                                                       n_group=2, topk_group=1, I=256, I_shared=256),
     "fp4_mixtral_large": _W["mixtral"].replace(name="fp4_mixtral_large", T=1100, h=256, I=256, dtype="nvfp4"),
-    # at least 128 rows per expert on average: the bf16 expert GEMMs run on CTA pairs (256-row tiles; a
-    # tail of at most 128 rows as a 128-row pair tile)
+    # at least 128 rows per expert on average and more full pair tiles than pairs: the bf16 expert GEMMs
+    # run on CTA pairs (256-row tiles; a tail of at most 128 rows as a 128-row pair tile)
     "pair_half_tiles": _W["dsv3_prefill"].replace(name="pair_half_tiles", T=600, h=512, E=16, k=4, n_group=4,
-                                                  topk_group=2, I=256, I_shared=256),
+                                                  topk_group=2, I=1280, I_shared=1280),
     "pair_mixtral": _W["mixtral"].replace(name="pair_mixtral", T=4500, h=512, I=384),
     "pair_dsv3": _W["dsv3_prefill"].replace(name="pair_dsv3", T=2600, h=512, E=8, k=4, n_group=2, topk_group=1,
                                             I=256, I_shared=256),
     "fp8_large_groups": _W["dsv3_fp8"].replace(name="fp8_large_groups", T=2200, h=512, E=8, k=4, n_group=2,
                                                topk_group=1, I=256, I_shared=256),
-    "pair_cap": _W["mixtral"].replace(name="pair_cap", T=4500, h=256, I=256, capacity_factor=1.0),
+    "pair_cap": _W["mixtral"].replace(name="pair_cap", T=4500, h=256, I=512, capacity_factor=1.0),
     # pairs with a shared expert and dropped slots
     "pair_cap_shared": _W["dsv3_prefill"].replace(name="pair_cap_shared", T=1500, h=256, E=8, k=4, n_group=2,
-                                                  topk_group=1, I=256, I_shared=256, capacity_factor=1.0),
+                                                  topk_group=1, I=512, I_shared=512, capacity_factor=1.0),
     # experts of more than 8 pair tiles (2250 rows): the tile order walks them in bands of 8 row tiles
-    "pair_bands": _W["mixtral"].replace(name="pair_bands", T=4500, h=256, E=4, I=256),
+    "pair_bands": _W["mixtral"].replace(name="pair_bands", T=4500, h=256, E=4, I=512),
 }
 
 
