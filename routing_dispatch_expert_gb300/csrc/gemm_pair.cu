@@ -52,6 +52,16 @@
 
 namespace moe {
 
+
+namespace {
+// 32-byte store (st.global.v8.b32): one full L2 sector per lane; the address must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+}  // namespace
+
 namespace g2 {
 
 constexpr int BM = 128;                 // rows per CTA
@@ -77,6 +87,7 @@ struct Args {
   const float* row_weight;
   int* status;
   int* tile_ctr;  // tile counter (zero before the launch), or nullptr: fixed stride
+  int vec32;      // the output rows and their column tiles start on 32-byte boundaries
   long long wait_limit;
 };
 
@@ -340,9 +351,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             p[i] = pack_bf16x2(h0, h1);
           }
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            if (args.vec32) {
+              st_global_v8(out + c, p);
+              st_global_v8(out + c + 16, p + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
         }
       } else {
@@ -360,9 +376,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 16; ++i)
             p[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * w, __uint_as_float(v[2 * i + 1]) * w);
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            if (args.vec32) {
+              st_global_v8(out + c, p);
+              st_global_v8(out + c + 16, p + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
         }
       }
@@ -451,6 +472,7 @@ cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t
   a.row_weight = d.row_weight;
   a.status = d.status;
   a.tile_ctr = d.tile_ctr;
+  a.vec32 = (reinterpret_cast<uintptr_t>(d.out) & 31) == 0 && ((int64_t)d.ldo * 2) % 32 == 0;
   a.wait_limit = 4000000000LL;  // about two seconds of SM clock
   cfg.gridDim = dim3(2 * max_pairs);
   e = cudaLaunchKernelEx(&cfg, g2::grouped_gemm_bf16_pair_kernel, tA, tB, tBs, tB64, tBs64, a);
