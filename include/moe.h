@@ -206,7 +206,9 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, 
  *     sizes return MOE_ERR_UNSUPPORTED before any work is enqueued;
  *   - allocates nothing: no cudaMalloc / cudaFree / allocating library routine;
  *   - the first call on a device looks up the array's device address on that device (set-up), so
- *     make that first call before any stream capture;
+ *     make that first call before any stream capture; the address belongs to the context current
+ *     on the device, so a call that finds another context there (after cudaDeviceReset, or with
+ *     another driver context made current) looks it up again, which is again a set-up call;
  *   - every call shares the one array, so calls that overlap on the GPU (other streams, other host
  *     threads) race and must be serialised by the caller;
  *   - a topk_idx entry outside [0, E) is skipped (inv_pos = -1) as in moe_dispatch, but the status

@@ -620,29 +620,26 @@ MOE_EXPORT int moe_combine(const moe_config* cfg, const void* yd, const int32_t*
 namespace {
 
 // A second stream per device for the shared expert, with the fork and join events. Created on first
-// use and kept for the life of the process; the enqueue of a fork ... join section holds the mutex,
-// so calls from several host threads cannot interleave their event records.
+// use on a device (and again under a new context there, e.g. after cudaDeviceReset) and kept for the
+// life of the process; the enqueue of a fork ... join section holds g_side_mu, so calls from several
+// host threads cannot interleave their event records.
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-constexpr int kMaxDevices = 64;
 std::mutex g_side_mu;
-SideStream g_side[kMaxDevices];
+moe::PerDevice<SideStream> g_side;
 
-cudaError_t side_stream(SideStream** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  SideStream& sd = g_side[dev];
-  if (!sd.stream) {
-    if ((e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-  }
-  *out = &sd;
-  return cudaSuccess;
+cudaError_t side_stream(SideStream* out) {
+  return moe::per_device<SideStream>(
+      g_side,
+      [](SideStream& sd) {
+        cudaError_t e;
+        if ((e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        return cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+      },
+      out);
 }
 
 }  // namespace
@@ -670,10 +667,11 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   // needs only x), overlapping dispatch and the routed GEMMs; the combine waits for it
   const bool side = cfg->I_shared > 0 && cfg->T > 0 && cfg->dtype == MOE_DTYPE_BF16;
   std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
-  SideStream* sd = nullptr;
+  SideStream side_handles;
+  SideStream* sd = &side_handles;
   if (side) {
     side_lock.lock();
-    if ((e = side_stream(&sd)) != cudaSuccess) return cuda_fail(e, "second stream set-up");
+    if ((e = side_stream(sd)) != cudaSuccess) return cuda_fail(e, "second stream set-up");
     if ((e = cudaEventRecord(sd->fork, s)) != cudaSuccess) return cuda_fail(e, "fork event record");
     if ((e = cudaStreamWaitEvent(sd->stream, sd->fork, 0)) != cudaSuccess) return cuda_fail(e, "fork wait");
     const int src = do_shared_ffn_bf16(cfg, weights, x, ws, L, sd->stream);
@@ -851,26 +849,24 @@ static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocStatusInts + 
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
-
-std::mutex g_noalloc_mu;
-int32_t* g_noalloc_addr[kNoAllocMaxDevices] = {};
+moe::PerDevice<int32_t*> g_noalloc_addr;
 
 // Device address of the scratch array on the current device. The name is only a host-side stand-in;
-// the address is looked up once per device, with that device current, on the first call there.
+// the address is looked up with the device current, on the first call there, and again when the
+// context current on the device has changed since (cudaDeviceReset, or another context made current),
+// since the array's address belongs to the module loaded into one context.
 int noalloc_scratch(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device ordinal beyond 63");
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static dispatch scratch");
-    g_noalloc_addr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_noalloc_addr[dev];
+  const cudaError_t e = moe::per_device<int32_t*>(
+      g_noalloc_addr,
+      [](int32_t*& addr) {
+        void* p = nullptr;
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        addr = static_cast<int32_t*>(p);
+        return r;
+      },
+      out);
+  if (e == cudaErrorInvalidDevice) return fail(MOE_ERR_UNSUPPORTED, "device ordinal beyond 63");
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static dispatch scratch");
   return MOE_OK;
 }
 

@@ -259,13 +259,19 @@ cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
   dp::scan_kernel<<<1, 1024, 0, stream>>>(d.scratch, nblk, d.E, cap, d.counts, d.offsets, d.n_slots, d.slot_expert,
                                           d.slot_replica, d.replicas, d.expert_counts);
   const size_t rank_smem = sizeof(uint32_t) * 2 * dp::WARPS * d.E;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(dp::rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(uint32_t) * 2 * dp::WARPS * 1024));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // the dynamic shared-memory opt-in (up to E = 1024) is a per-device function attribute
+  static PerDevice<bool> attr;
+  bool attr_set = false;
+  cudaError_t ae = per_device<bool>(
+      attr,
+      [](bool& v) {
+        const cudaError_t r = cudaFuncSetAttribute(dp::rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)(sizeof(uint32_t) * 2 * dp::WARPS * 1024));
+        v = r == cudaSuccess;
+        return r;
+      },
+      &attr_set);
+  if (ae != cudaSuccess) return ae;
   dp::rank_kernel<<<nblk, dp::TPB, rank_smem, stream>>>(d.topk_idx, d.topk_w, d.scratch, d.offsets, d.T, d.k, d.E,
                                                          cap, d.inv_pos, d.row_token, d.row_weight, d.n_slots,
                                                          d.max_replicas, d.replicas, d.replica_slot);

@@ -438,14 +438,42 @@ bool tma_encode_3d_plain(CUtensorMap* m, const void* base, int64_t G, int64_t ro
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+using PFN_ctx_get_current = CUresult (*)(CUcontext*);
+PFN_ctx_get_current g_ctx_get_current = nullptr;
+std::once_flag g_ctx_once;
+}  // namespace
+
+cudaError_t current_device(int* dev, const void** ctx) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PFN_ctx_get_current>(fn);
+  });
+  CUcontext c = nullptr;
+  if (!g_ctx_get_current || g_ctx_get_current(&c) != CUDA_SUCCESS) c = nullptr;
+  *ctx = c;
+  return cudaSuccess;
+}
+
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMsHint;
-  }
-  return n;
+  static PerDevice<int> table;
+  int n = 0;
+  const cudaError_t e = per_device<int>(
+      table,
+      [](int& v) {
+        int dev = 0;
+        cudaError_t r = cudaGetDevice(&dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess && v <= 0) r = cudaErrorInvalidValue;
+        return r;
+      },
+      &n);
+  return e == cudaSuccess ? n : kNumSMsHint;
 }
 
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err) {
@@ -454,18 +482,24 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
     *err = "cuTensorMapEncodeTiled is not available from the driver";
     return e;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel<gg::THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gg::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel<gg::ROUTER_THREADS>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
-    if (e != cudaSuccess) {
-      *err = "cudaFuncSetAttribute failed";
-      return e;
-    }
-    attr_set = true;
+  // the dynamic shared-memory opt-in is a per-device function attribute
+  static PerDevice<bool> attr;
+  bool attr_set = false;
+  e = per_device<bool>(
+      attr,
+      [](bool& v) {
+        cudaError_t r = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel<gg::THREADS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
+        if (r == cudaSuccess)
+          r = cudaFuncSetAttribute(gg::grouped_gemm_bf16_kernel<gg::ROUTER_THREADS>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
+        v = r == cudaSuccess;
+        return r;
+      },
+      &attr_set);
+  if (e != cudaSuccess) {
+    *err = "cudaFuncSetAttribute failed";
+    return e;
   }
   CUtensorMap tA, tB, tBs;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

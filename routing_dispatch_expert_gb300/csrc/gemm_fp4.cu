@@ -430,15 +430,21 @@ cudaError_t launch_grouped_gemm_nvfp4(const GroupedGemmFp4Desc& d, cudaStream_t 
     *err = "cuTensorMapEncodeTiled is not available from the driver";
     return e;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(g4::grouped_gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             g4::SMEM_BYTES);
-    if (e != cudaSuccess) {
-      *err = "cudaFuncSetAttribute failed";
-      return e;
-    }
-    attr_set = true;
+  // the dynamic shared-memory opt-in is a per-device function attribute
+  static PerDevice<bool> attr;
+  bool attr_set = false;
+  e = per_device<bool>(
+      attr,
+      [](bool& v) {
+        const cudaError_t r =
+            cudaFuncSetAttribute(g4::grouped_gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g4::SMEM_BYTES);
+        v = r == cudaSuccess;
+        return r;
+      },
+      &attr_set);
+  if (e != cudaSuccess) {
+    *err = "cudaFuncSetAttribute failed";
+    return e;
   }
   const int64_t G = d.n_experts > 0 ? d.n_experts : d.E;
   CUtensorMap tA, tA64, tQ, tS, tQs, tSs;

@@ -420,15 +420,21 @@ cudaError_t launch_grouped_gemm_fp8(const GroupedGemmFp8Desc& d, cudaStream_t st
     *err = "cuTensorMapEncodeTiled is not available from the driver";
     return e;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(g8::grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             g8::SMEM_BYTES);
-    if (e != cudaSuccess) {
-      *err = "cudaFuncSetAttribute failed";
-      return e;
-    }
-    attr_set = true;
+  // the dynamic shared-memory opt-in is a per-device function attribute
+  static PerDevice<bool> attr;
+  bool attr_set = false;
+  e = per_device<bool>(
+      attr,
+      [](bool& v) {
+        const cudaError_t r =
+            cudaFuncSetAttribute(g8::grouped_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g8::SMEM_BYTES);
+        v = r == cudaSuccess;
+        return r;
+      },
+      &attr_set);
+  if (e != cudaSuccess) {
+    *err = "cudaFuncSetAttribute failed";
+    return e;
   }
   CUtensorMap tA, tB, tBs;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;

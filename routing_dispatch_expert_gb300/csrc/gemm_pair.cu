@@ -415,7 +415,6 @@ cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t
     *err = "cuTensorMapEncodeTiled is not available from the driver";
     return e;
   }
-  static int max_pairs = 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -427,22 +426,29 @@ cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_pairs == 0) {
-    e = cudaFuncSetAttribute(g2::grouped_gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             g2::SMEM_BYTES);
-    if (e != cudaSuccess) {
-      *err = "cudaFuncSetAttribute failed";
-      return e;
-    }
-    // as many pairs as can be resident at once (SMs of a GPC pair up; an odd one stays out)
-    cfg.gridDim = dim3(2 * (num_sms() / 2));
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, g2::grouped_gemm_bf16_pair_kernel, &cfg);
-    if (e != cudaSuccess || n <= 0) {
-      *err = "cudaOccupancyMaxActiveClusters failed for the CTA-pair grouped GEMM";
-      return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-    }
-    max_pairs = n < num_sms() / 2 ? n : num_sms() / 2;
+  // the shared-memory opt-in and the resident-cluster count are per device
+  static PerDevice<int> pairs_table;
+  int max_pairs = 0;
+  e = per_device<int>(
+      pairs_table,
+      [&cfg](int& v) {
+        cudaError_t r = cudaFuncSetAttribute(g2::grouped_gemm_bf16_pair_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, g2::SMEM_BYTES);
+        if (r != cudaSuccess) return r;
+        // as many pairs as can be resident at once (SMs of a GPC pair up; an odd one stays out)
+        cudaLaunchConfig_t probe = cfg;
+        probe.gridDim = dim3(2 * (num_sms() / 2));
+        int n = 0;
+        r = cudaOccupancyMaxActiveClusters(&n, g2::grouped_gemm_bf16_pair_kernel, &probe);
+        if (r != cudaSuccess) return r;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+        v = n < num_sms() / 2 ? n : num_sms() / 2;
+        return cudaSuccess;
+      },
+      &max_pairs);
+  if (e != cudaSuccess) {
+    *err = "cudaFuncSetAttribute / cudaOccupancyMaxActiveClusters failed for the CTA-pair grouped GEMM";
+    return e;
   }
   CUtensorMap tA, tB, tBs, tB64, tBs64;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -6,9 +6,26 @@
 
 #include <string>
 
+#include "device_state.h"
+
 namespace moe {
 
+// SM count of the current device (per device; set up on first use there).
 int num_sms();
+
+// The current device and the driver context current on this thread (nullptr if none yet).
+cudaError_t current_device(int* dev, const void** ctx);
+
+// table's value for the current device and context, set up by init(T&) -> cudaError_t on first use.
+template <class T, class Init>
+cudaError_t per_device(PerDevice<T>& table, Init&& init, T* out) {
+  int dev = 0;
+  const void* ctx = nullptr;
+  cudaError_t e = current_device(&dev, &ctx);
+  if (e != cudaSuccess) return e;
+  const int rc = table.get(dev, ctx, [&](T& v) { return static_cast<int>(init(v)); }, out);
+  return rc == -1 ? cudaErrorInvalidDevice : static_cast<cudaError_t>(rc);
+}
 
 // EPLB placement plan on the host (eplb.cu).
 int eplb_plan(const int64_t* load, int E, int n_cards, int n_redundant, int32_t* replicas, int32_t* slot_expert,
