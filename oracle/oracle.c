@@ -477,39 +477,56 @@ ORC_API void orc_expert_ffn_bf16(const uint16_t* x, int64_t m, int64_t h, int64_
 }
 
 /* FP8 block-scaled variant ([PPLX] "Quantization"): operands are e4m3 codes with fp32
- * scales; values are code * scale. xq: [m, h], xs: [m, h/128]; w_gu_q: [2I, h] with
- * w_gu_s: [2I/128, h/128]; w_d_q: [h, I] with w_d_s: [h/128, I/128]. The SwiGLU product is
- * quantised 1x128 along I ([PPLX]: SiLU output block-quantised with a 128-element amax) and
- * dequantised before the down projection. */
+ * scales; a value is code * scale. xq: [m, h], xs: [m, h/128]; w_gu_q: [2I, h] with
+ * w_gu_s: [2I/128, h/128]; w_d_q: [h, I] with w_d_s: [h/128, I/128]. Every operand is first
+ * dequantised to its value (exact in fp64: a 4-bit significand times a 24-bit one), then the
+ * FFN runs on the values in fp64 as in the bf16 layer. The SwiGLU product is quantised 1x128
+ * along I ([PPLX]: SiLU output block-quantised with a 128-element amax) and dequantised before
+ * the down projection. */
 ORC_API void orc_expert_ffn_fp8(const uint8_t* xq, const float* xs, int64_t m, int64_t h, int64_t I,
                                 const uint8_t* w_gu_q, const float* w_gu_s, const uint8_t* w_d_q,
                                 const float* w_d_s, double* out) {
   int64_t hb = h / 128, ib = I / 128;
+  double* wgu = (double*)malloc(sizeof(double) * 2 * I * h);
+  double* wd = (double*)malloc(sizeof(double) * h * I);
+  double* xv = (double*)malloc(sizeof(double) * h);
   double* a = (double*)malloc(sizeof(double) * I);
+  double* av = (double*)malloc(sizeof(double) * I);
   uint8_t* aq = (uint8_t*)malloc(I);
   float* as = (float*)malloc(sizeof(float) * ib);
+#pragma omp parallel for schedule(static)
+  for (int64_t c = 0; c < 2 * I; ++c)
+    for (int64_t d = 0; d < h; ++d)
+      wgu[c * h + d] = orc_e4m3_decode(w_gu_q[c * h + d]) * (double)w_gu_s[(c / 128) * hb + d / 128];
+#pragma omp parallel for schedule(static)
+  for (int64_t d = 0; d < h; ++d)
+    for (int64_t c = 0; c < I; ++c)
+      wd[d * I + c] = orc_e4m3_decode(w_d_q[d * I + c]) * (double)w_d_s[(d / 128) * ib + c / 128];
   for (int64_t r = 0; r < m; ++r) {
+    for (int64_t d = 0; d < h; ++d) xv[d] = orc_e4m3_decode(xq[r * h + d]) * (double)xs[r * hb + d / 128];
 #pragma omp parallel for schedule(static)
     for (int64_t c = 0; c < I; ++c) {
       double g = 0.0, u = 0.0;
       for (int64_t d = 0; d < h; ++d) {
-        double xv = orc_e4m3_decode(xq[r * h + d]) * (double)xs[r * hb + d / 128];
-        g += xv * orc_e4m3_decode(w_gu_q[c * h + d]) * (double)w_gu_s[(c / 128) * hb + d / 128];
-        u += xv * orc_e4m3_decode(w_gu_q[(I + c) * h + d]) * (double)w_gu_s[((I + c) / 128) * hb + d / 128];
+        g += xv[d] * wgu[c * h + d];
+        u += xv[d] * wgu[(I + c) * h + d];
       }
       a[c] = orc_silu(g) * u;
     }
     orc_quant_1x128(a, 1, I, aq, as);
+    for (int64_t c = 0; c < I; ++c) av[c] = orc_e4m3_decode(aq[c]) * (double)as[c / 128];
 #pragma omp parallel for schedule(static)
     for (int64_t d = 0; d < h; ++d) {
       double o = 0.0;
-      for (int64_t c = 0; c < I; ++c)
-        o += orc_e4m3_decode(aq[c]) * (double)as[c / 128] * orc_e4m3_decode(w_d_q[d * I + c]) *
-             (double)w_d_s[(d / 128) * ib + c / 128];
+      for (int64_t c = 0; c < I; ++c) o += av[c] * wd[d * I + c];
       out[r * h + d] = o;
     }
   }
+  free(wgu);
+  free(wd);
+  free(xv);
   free(a);
+  free(av);
   free(aq);
   free(as);
 }
