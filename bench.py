@@ -7,8 +7,14 @@ GEMMs, combine) over one batch of synthetic tokens, through the C ABI (moe_forwa
 workload is the DeepSeek-V3-shaped prefill layer (16384 tokens, h 7168, 256 routed experts top-8 +
 1 shared, intermediate 2048); its 22.6 GB of expert weights are read every step, far more than L2.
 
-Prints ONE JSON line on rank 0. ``--impl reference`` times the CPU oracle instead (on the host cores,
-bounded samples of the same workload, nothing on the GPU).
+Prints ONE JSON line on rank 0. The headline fields are the default workload's; on one GPU the line
+also carries ``sustained`` (the same step back to back for about 3 s, with its own clock samples) and
+``per_config``: the same measurements for every other configuration of the layer (tiny, Mixtral-shaped,
+DeepSeek-V3-shaped decode, FP8 and decode with NVFP4 expert weights), each with its tokens/s, layer
+roofline fraction, expert-GEMM roofline, CUDA-graph and end-to-end rates, clocks and CPU-oracle rate.
+Configurations whose weights and activations fit in L2 (tiny) are timed with L2 flushed between steps.
+``--impl reference`` times the CPU oracle instead (on the host cores, bounded samples of the same
+workload, nothing on the GPU).
 """
 from __future__ import annotations
 
@@ -248,7 +254,8 @@ def reference_arm(args, wl, rank, world):
         "warmup": args.warmup, "ms_per_step": float(np.median(secs)) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl, world),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": omp_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": omp_threads(), "cpu_model": cpu_model(),
+                         "kind": "oracle",
                          "sample": f"per step {int(np.median(samples))} of the workload's tokens through the whole "
                                    "oracle layer (routed rows evaluated with one expert's weights, same shapes)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -301,58 +308,31 @@ def measure_fp8_peak(n=8192, sustain_s=4.0):
                                      f"(burst) and {reps} back to back (sustained)"}), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="dsv3_prefill")
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--tokens", type=int, default=None, help="override T (small profiling cases)")
-    ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
-    ap.add_argument("--fp8-peak", action="store_true",
-                    help="measure the library FP8 GEMM rate (cuBLASLt through torch._scaled_mm) and exit")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    if args.fp8_peak:
-        measure_fp8_peak()
-        return
+PER_CONFIG = ("tiny", "mixtral", "dsv3_decode", "dsv3_fp8", "dsv3_decode_fp4")
 
-    import synth
 
-    wl = synth.WORKLOADS[args.workload]
-    if args.tokens is not None or args.experts is not None:
-        wl = wl.replace(name=f"{wl.name}_T{args.tokens or wl.T}_E{args.experts or wl.E}", T=args.tokens or wl.T,
-                        E=args.experts or wl.E)
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+def cpu_model():
+    """The host CPU's model name (lscpu on Arm, /proc/cpuinfo elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
 
-    if args.impl == "reference":
-        reference_arm(args, wl, rank, world)
-        return
+    return platform.machine()
 
-    import torch
 
-    import routing_dispatch_expert_gb300 as rde
-    from routing_dispatch_expert_gb300 import build as pkg_build
-
-    torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    if rank == 0 or world > 1:
-        pkg_build.build()
-        synth.build()
-    if dist is not None:
-        dist.barrier()
-    rde.load()
-
-    dev = torch.device("cuda", local_rank)
+def make_layer(wl, dev, rde, synth, torch):
+    """Config, device weights (FP8 / NVFP4 quantised by the library), workspace and x/y buffers."""
     cfg = rde.make_config(T=wl.T, h=wl.h, E=wl.E, k=wl.k, I=wl.I, I_shared=wl.I_shared, n_group=wl.n_group,
                           topk_group=wl.topk_group, score=wl.score, renorm=wl.renorm, routed_scale=wl.routed_scale,
                           dtype=wl.dtype)
@@ -372,23 +352,66 @@ def main():
     weights = rde.Weights(w_router=inp["w_router"], bias=inp["bias"], **wts)
     ws = rde.alloc_workspace(cfg, dev)
     rde.device_status(cfg, ws)
-    x = inp["x"]
+    return cfg, weights, ws, inp["x"]
+
+
+def fits_in_l2(wl, props):
+    """True when a step's weights and activations could stay in L2 between steps (then L2 is flushed)."""
+    w = 3.0 * wl.h * wl.I * (wl.E + (1 if wl.has_shared else 0)) * weight_bytes(wl)
+    return w + 4.0 * wl.T * wl.h < 2 * getattr(props, "L2_cache_size", 129 << 20)
+
+
+class Timer:
+    """Mean milliseconds of `steps` calls of fn on `stream`, CUDA events on that stream. Without a
+    flush buffer the calls run back to back between one pair of events; with one, every call has its
+    own pair of events and the buffer (larger than L2) is overwritten between calls, outside them."""
+
+    def __init__(self, torch, stream, flush=None):
+        self.torch, self.stream, self.flush = torch, stream, flush
+
+    def __call__(self, fn, steps):
+        torch, stream = self.torch, self.stream
+        if self.flush is None:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / steps
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            with torch.cuda.stream(stream):
+                self.flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+
+def measure(wl, args, dev, dist, rde, synth, torch, steps, gpu_index, sustain_s=0.0):
+    """One workload: K timed moe_forward steps (the metric), the same steps through the step entry
+    points with the expert-GEMM pair bracketed by events (its roofline), one CUDA graph per step, the
+    end-to-end rate from pinned host buffers, and the roofline of the layer. Returns a dict."""
+    props = torch.cuda.get_device_properties(dev)
+    cfg, weights, ws, x = make_layer(wl, dev, rde, synth, torch)
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream(dev)
+    flush = None
+    if fits_in_l2(wl, props):
+        flush = torch.empty(4 * getattr(props, "L2_cache_size", 129 << 20), dtype=torch.uint8, device=dev)
+    timer = Timer(torch, stream, flush)
 
-    # warm-up (untimed)
     for _ in range(args.warmup):
         rde.forward(cfg, x, weights, y, ws)
     torch.cuda.synchronize(dev)
     status = rde.device_status(cfg, ws)
     if status != 0:
-        raise SystemExit(f"device status {status} after warm-up")
+        raise SystemExit(f"{wl.name}: device status {status} after warm-up")
     bal = rde.balance(cfg, ws)
     active = bal["active"]
 
-    # timed region: K whole-layer steps; the grouped-GEMM pair (moe_expert_ffn) is timed separately
-    # on the same stream by running the steps through their own entry points
-    lay = rde.workspace_layout(cfg)
     R = wl.T * wl.k
     R_tot = R + (wl.T if wl.has_shared else 0)
     v = lambda name, dt, shape: rde.ws_view(ws, cfg, name, dt, shape)  # noqa: E731
@@ -400,49 +423,39 @@ def main():
               xd=v("xd", xd_dt, (R_tot, wl.h)), yd=v("yd", torch.bfloat16, (R_tot, wl.h)))
     xs = v("xd_scales", torch.float32, (R_tot, wl.h // 128)) if wl.dtype == "fp8" else None
 
-    def step_split(ev_a, ev_b):
-        rde.route(cfg, x, weights, it["idx"], it["w"], logits=it["logits"], ws=ws)
-        rde.dispatch(cfg, x, it["idx"], it["w"], it["counts"], it["offsets"], it["inv_pos"], it["row_token"],
-                     it["row_weight"], it["xd"], xs, ws)
-        ev_a.record(stream)
-        rde.expert_ffn(cfg, weights, it["xd"], xs, it["offsets"], it["row_weight"], it["yd"], ws)
-        ev_b.record(stream)
-        rde.combine(cfg, it["yd"], it["inv_pos"], y)
-
-    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] if world == 1 else local_rank
-    # timed region (the headline): K steps of moe_forward, the public fused entry point
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # timed region (the metric): K steps of moe_forward, the public fused entry point
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index) as clk:
         n0 = rde.launch_count()
-        start.record(stream)
-        for _ in range(args.steps):
-            rde.forward(cfg, x, weights, y, ws)
-        end.record(stream)
-        torch.cuda.synchronize(dev)
+        ms_step = timer(lambda: rde.forward(cfg, x, weights, y, ws), steps)
         n1 = rde.launch_count()
         if dist is not None:
             dist.barrier()
     clocks = clk.summary()
-    ms_step = start.elapsed_time(end) / args.steps
-    ms_fwd = ms_step
 
     # the same steps through the step entry points, with the expert-GEMM pair (moe_expert_ffn)
-    # bracketed by events on the same stream: the roofline's timing
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # bracketed by its own events on the same stream: the roofline's timing
+    gemm_times = []
+
+    def step_split():
+        rde.route(cfg, x, weights, it["idx"], it["w"], logits=it["logits"], ws=ws)
+        rde.dispatch(cfg, x, it["idx"], it["w"], it["counts"], it["offsets"], it["inv_pos"], it["row_token"],
+                     it["row_weight"], it["xd"], xs, ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rde.expert_ffn(cfg, weights, it["xd"], xs, it["offsets"], it["row_weight"], it["yd"], ws)
+        b.record(stream)
+        gemm_times.append((a, b))
+        rde.combine(cfg, it["yd"], it["inv_pos"], y)
+
     for _ in range(2):
-        step_split(*evs[0])
+        step_split()
     torch.cuda.synchronize(dev)
-    sp_s, sp_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sp_s.record(stream)
-    for i in range(args.steps):
-        step_split(*evs[i])
-    sp_e.record(stream)
-    torch.cuda.synchronize(dev)
-    ms_split = sp_s.elapsed_time(sp_e) / args.steps
-    gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    gemm_times.clear()
+    ms_split = timer(step_split, steps)
+    gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in gemm_times]))
 
     # the same layer as one CUDA graph per step (moe_graph_*): launch cost removed
     gstream = torch.cuda.Stream(dev)
@@ -451,70 +464,85 @@ def main():
         graph = rde.Graph(cfg, x, weights, y, ws, gstream)
         for _ in range(2):
             graph.launch()
-        g_s, g_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         gstream.synchronize()
-        g_s.record(gstream)
-        for _ in range(args.steps):
-            graph.launch()
-        g_e.record(gstream)
+        ms_graph = Timer(torch, gstream, flush)(graph.launch, steps)
     gstream.synchronize()
-    ms_graph = g_s.elapsed_time(g_e) / args.steps
     del graph
 
     # end to end through the public API with host buffers: every step copies its x in from pinned host
-    # memory and its y out to pinned host memory. The copies run on their own streams with two device
-    # buffers of x and y alternating, so the copy-in of step i+1 and the copy-out of step i-1 overlap
-    # the layer of step i (the way a serving loop feeds a layer).
+    # memory and its y out to pinned host memory. With inputs larger than L2 the copies run on their own
+    # streams with two device buffers of x and y alternating, so the copy-in of step i+1 and the copy-out
+    # of step i-1 overlap the layer of step i (the way a serving loop feeds a layer); when L2 is flushed
+    # between steps, each step is the copy-in, the layer and the copy-out in sequence.
     x_host = x.cpu().pin_memory()
     y_host = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
     x_dev = [torch.empty_like(x) for _ in range(2)]
     y_dev = [y, torch.empty_like(y)]
-    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]  # x_dev[b] holds the step's input
-    ev_used = [torch.cuda.Event() for _ in range(2)]  # the layer has read x_dev[b] and written y_dev[b]
-    ev_out = [torch.cuda.Event() for _ in range(2)]  # y_dev[b] is on the host
+    e2e_steps = max(4, steps // 2)
+    if flush is not None:
+        def e2e_seq():
+            x_dev[0].copy_(x_host, non_blocking=True)
+            rde.forward(cfg, x_dev[0], weights, y_dev[0], ws)
+            y_host[0].copy_(y_dev[0], non_blocking=True)
 
-    def e2e_step(i):
-        b = i & 1
-        if i >= 2:
-            h2d.wait_event(ev_used[b])
-        with torch.cuda.stream(h2d):
-            x_dev[b].copy_(x_host, non_blocking=True)
-        ev_in[b].record(h2d)
-        stream.wait_event(ev_in[b])
-        if i >= 2:
-            stream.wait_event(ev_out[b])
-        rde.forward(cfg, x_dev[b], weights, y_dev[b], ws)
-        ev_used[b].record(stream)
-        d2h.wait_event(ev_used[b])
-        with torch.cuda.stream(d2h):
-            y_host[b].copy_(y_dev[b], non_blocking=True)
-        ev_out[b].record(d2h)
+        e2e_seq()
+        torch.cuda.synchronize(dev)
+        ms_e2e = timer(e2e_seq, e2e_steps)
+    else:
+        h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_used = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    e2e_steps = max(4, args.steps // 2)
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_s.record(stream)
-    h2d.wait_stream(stream)
-    d2h.wait_stream(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    stream.wait_event(ev_out[0])
-    stream.wait_event(ev_out[1])
-    e_e.record(stream)
-    torch.cuda.synchronize(dev)
-    ms_e2e = e_s.elapsed_time(e_e) / e2e_steps
+        def e2e_step(i):
+            b = i & 1
+            if i >= 2:
+                h2d.wait_event(ev_used[b])
+            with torch.cuda.stream(h2d):
+                x_dev[b].copy_(x_host, non_blocking=True)
+            ev_in[b].record(h2d)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])
+            rde.forward(cfg, x_dev[b], weights, y_dev[b], ws)
+            ev_used[b].record(stream)
+            d2h.wait_event(ev_used[b])
+            with torch.cuda.stream(d2h):
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+            ev_out[b].record(d2h)
+
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_s.record(stream)
+        h2d.wait_stream(stream)
+        d2h.wait_stream(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        stream.wait_event(ev_out[0])
+        stream.wait_event(ev_out[1])
+        e_e.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = e_s.elapsed_time(e_e) / e2e_steps
+
+    # a sustained window: back-to-back moe_forward steps for `sustain_s` seconds, with its own clocks
+    sustained = None
+    if sustain_s > 0:
+        n_sus = max(steps, int(np.ceil(sustain_s * 1e3 / ms_step)))
+        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_index) as clk2:
+            ms_sus = timer(lambda: rde.forward(cfg, x, weights, y, ws), n_sus)
+        sustained = {"steps": n_sus, "seconds": n_sus * ms_sus * 1e-3, "ms_per_step": ms_sus, "clocks": clk2.summary()}
 
     ms_step, ms_e2e, gemm_ms, ms_graph, ms_split = max_over_ranks([ms_step, ms_e2e, gemm_ms, ms_graph, ms_split], dist,
                                                                   dev)
     status = rde.device_status(cfg, ws)
     if status != 0:
-        raise SystemExit(f"device status {status} after the timed region")
+        raise SystemExit(f"{wl.name}: device status {status} after the timed region")
 
     peaks, peaks_kind = load_peaks()
-    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_sms = props.multi_processor_count
     flops, gemm_flops, bytes_ = layer_counts(wl, active)
     p_tc = peaks["bf16_tflops"] * 1e12
     p_hbm = peaks["hbm_gbs"] * 1e9
@@ -552,37 +580,137 @@ def main():
                               else f"bf16 burst, {peaks_kind}"),
                 "frac_of_sustained": gemm_tflops / gemm_peak_sus,
                 "timing": "moe_expert_ffn inside the step-entry-point path, CUDA events on the launching stream"}
+    world = 1 if dist is None else dist.get_world_size()
+    out = {
+        "workload": wl.name, "steps": steps, "ms_per_step": ms_step, "value": job_tokens_per_s(world, wl.T, ms_step),
+        "unit": UNIT,
+        "l2": ("flushed between steps (a buffer of 4 x L2 overwritten outside the timed events)" if flush is not None
+               else "inputs larger than L2: every step reads all active expert weights (GBs) once"),
+        "roofline": roof,
+        "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3), "flops": flops,
+                           "bytes": bytes_, "active_experts": active, "bound": "hbm" if hbm_bound else "tensor",
+                           "peaks": peaks_kind},
+        "balance": {"max_over_mean": bal["max_over_mean"], "active_experts": bal["active"],
+                    "dropped_assignments": bal["dropped"]},
+        "ms_moe_forward": ms_step, "ms_split_step": ms_split, "ms_expert_ffn": gemm_ms,
+        "graph": {"value": job_tokens_per_s(world, wl.T, ms_graph), "unit": UNIT, "ms_per_step": ms_graph,
+                  "note": "the same step replayed as one CUDA graph (moe_graph_launch)"},
+        "e2e": {"value": job_tokens_per_s(world, wl.T, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(y.numel() * y.element_size())},
+        "gpu_launches": int(n1 - n0), "launches_per_step": (n1 - n0) / steps,
+        "clocks": clocks,
+    }
+    if sustained is not None:
+        sustained["value"] = job_tokens_per_s(world, wl.T, sustained["ms_per_step"])
+        sustained["unit"] = UNIT
+        sustained["layer_roofline_frac"] = t_roof / (sustained["ms_per_step"] * 1e-3)
+        out["sustained"] = sustained
+    del cfg, weights, ws, x, y, it, xs, flush, x_host, y_host, x_dev, y_dev
+    import gc
+
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline_of(wl, budget_s):
+    v_cpu, S, dt = time_cpu_oracle(wl, budget_s)
+    return {"value": v_cpu, "unit": UNIT, "cores": omp_threads(), "cpu_model": cpu_model(), "kind": "oracle",
+            "sample": f"{S} of the workload's tokens through the whole oracle layer in {dt:.1f} s "
+                      "(routed rows evaluated with one expert's weights, same shapes)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="dsv3_prefill")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time only the headline workload")
+    ap.add_argument("--sustain", type=float, default=3.0, help="seconds of the sustained window (0: none)")
+    ap.add_argument("--tokens", type=int, default=None, help="override T (small profiling cases)")
+    ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
+    ap.add_argument("--fp8-peak", action="store_true",
+                    help="measure the library FP8 GEMM rate (cuBLASLt through torch._scaled_mm) and exit")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.fp8_peak:
+        measure_fp8_peak()
+        return
+
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    small = args.tokens is not None or args.experts is not None
+    if small:
+        wl = wl.replace(name=f"{wl.name}_T{args.tokens or wl.T}_E{args.experts or wl.E}", T=args.tokens or wl.T,
+                        E=args.experts or wl.E)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, wl, rank, world)
+        return
+
+    import torch
+
+    import routing_dispatch_expert_gb300 as rde
+    from routing_dispatch_expert_gb300 import build as pkg_build
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0 or world > 1:
+        pkg_build.build()
+        synth.build()
+    if dist is not None:
+        dist.barrier()
+    rde.load()
+    dev = torch.device("cuda", local_rank)
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] if world == 1 else local_rank
+
+    head = measure(wl, args, dev, dist, rde, synth, torch, args.steps, gpu_index,
+                   sustain_s=0.0 if small else args.sustain)
+    # every other configuration of the layer, one after another on the same GPU (1-GPU runs only)
+    per_config = {}
+    if world == 1 and not small and not args.no_per_config:
+        for name in PER_CONFIG:
+            if name == wl.name:
+                continue
+            w2 = synth.WORKLOADS[name]
+            # sub-millisecond steps: more of them, so the timed region is not a few microseconds
+            per_config[name] = measure(w2, args, dev, dist, rde, synth, torch, args.steps, gpu_index)
+            if per_config[name]["ms_per_step"] < 1.0:
+                per_config[name] = measure(w2, args, dev, dist, rde, synth, torch, args.steps * 25, gpu_index)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v_cpu, S, dt = time_cpu_oracle(wl, 12.0)
-        cpu = {"value": v_cpu, "unit": UNIT, "cores": omp_threads(), "kind": "oracle",
-               "sample": f"{S} of the workload's tokens through the whole oracle layer in {dt:.1f} s "
-                         "(routed rows evaluated with one expert's weights, same shapes)"}
+        cpu = cpu_baseline_of(wl, 12.0)
+        for name, entry in per_config.items():
+            entry["cpu_baseline"] = cpu_baseline_of(synth.WORKLOADS[name], 3.0)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": job_tokens_per_s(world, wl.T, ms_step), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if wl.dtype == "fp8" else "bf16",
             "data": "synthetic", "config": config_of(wl, world),
-            "roofline": roof,
-            "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3), "flops": flops,
-                               "bytes": bytes_, "active_experts": active,
-                               "bound": "hbm" if hbm_bound else "tensor",
-                               "peaks": peaks_kind},
-            "balance": {"max_over_mean": bal["max_over_mean"], "active_experts": bal["active"],
-                        "dropped_assignments": bal["dropped"]},
-            "ms_moe_forward": ms_fwd, "ms_split_step": ms_split, "ms_expert_ffn": gemm_ms,
-            "graph": {"value": job_tokens_per_s(world, wl.T, ms_graph), "unit": UNIT, "ms_per_step": ms_graph,
-                      "note": "the same step replayed as one CUDA graph (moe_graph_launch)"},
-            "e2e": {"value": job_tokens_per_s(world, wl.T, ms_e2e), "unit": UNIT,
-                    "h2d_bytes_per_step": int(x.numel() * x.element_size()),
-                    "d2h_bytes_per_step": int(y.numel() * y.element_size())},
-            "gpu_launches": int(n1 - n0),
-            "clocks": clocks,
-            "cpu_baseline": cpu,
         }
+        for key in ("roofline", "layer_roofline", "balance", "ms_moe_forward", "ms_split_step", "ms_expert_ffn",
+                    "graph", "e2e", "gpu_launches", "clocks", "sustained"):
+            if key in head:
+                line[key] = head[key]
+        line["cpu_baseline"] = cpu
+        if per_config:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

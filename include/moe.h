@@ -299,6 +299,28 @@ int moe_quantize_weights_nvfp4(const void* w, int64_t batch, int64_t rows, int64
 int moe_eplb_plan(const int64_t* load, int32_t E, int32_t n_cards, int32_t n_redundant, int32_t* replicas,
                   int32_t* slot_expert, int32_t* slot_replica, int32_t* replica_slot, double* card_load);
 
+/* Load balance of the last step run with a workspace (inference guide 6.4, section 5.1: an
+ * expert-parallel step waits for its busiest expert; Ultralytics "Load balancing and capacity": a
+ * capacity limit drops the assignments beyond it). Computed on the device from the counts and
+ * offsets that the last moe_forward or moe_dispatch with this workspace left in it, and written to
+ * `stats`, a caller-owned DEVICE buffer of one moe_balance_stats (16-byte aligned); asynchronous on
+ * `stream` like every other call. Under a placement the counts are per physical slot.
+ *   max_rows       rows of the busiest expert (slot)
+ *   active         experts (slots) with at least one row
+ *   kept           rows kept, offsets[S] (T*k when dropless)
+ *   dropped        T*k - kept: assignments a capacity limit dropped
+ *   max_over_mean  max_rows / (kept / S), rounded once to fp32 (0 when kept == 0); S = E, or n_slots
+ * Errors: MOE_ERR_INVALID, MOE_ERR_CUDA. */
+typedef struct {
+  int32_t max_rows;
+  int32_t active;
+  int32_t kept;
+  int32_t dropped;
+  float max_over_mean;
+  int32_t reserved[3];
+} moe_balance_stats;
+int moe_balance(const moe_config* cfg, const void* ws, moe_balance_stats* stats, moe_stream_t stream);
+
 /* Device status word of a workspace: waits for `stream`, then reads the MOE_STATUS_* bits that
  * kernels of earlier calls with this workspace set into *status, and clears them. moe_forward clears
  * the word at its start; the step entry points only add bits, so a new workspace (arbitrary

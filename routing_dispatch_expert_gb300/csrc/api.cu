@@ -815,6 +815,20 @@ MOE_EXPORT int moe_selftest_wait_timeout(const moe_config* cfg, void* ws, size_t
   return MOE_OK;
 }
 
+MOE_EXPORT int moe_balance(const moe_config* cfg, const void* ws, moe_balance_stats* stats, moe_stream_t stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  REQUIRE_PTR(ws, "ws");
+  REQUIRE_PTR(stats, "stats");
+  Layout L = make_layout(cfg);
+  void* w = const_cast<void*>(ws);
+  cudaError_t e = moe::launch_balance(at<int32_t>(w, L.l.counts), at<int32_t>(w, L.l.offsets), (int)n_groups(cfg),
+                                      (int64_t)cfg->T * cfg->k, stats, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "balance launch");
+  counted(1);
+  return MOE_OK;
+}
+
 MOE_EXPORT int moe_device_status(const moe_config* cfg, void* ws, int32_t* status, moe_stream_t stream) {
   int rc = check_config(cfg);
   if (rc) return rc;

@@ -240,7 +240,43 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict
   }
 }
 
+// Load balance of one step from its counts (S <= 1024 experts or slots): the busiest expert's rows,
+// the experts with rows, the kept rows (offsets[S]) and the dropped assignments, and busiest / mean.
+__global__ void __launch_bounds__(1024) balance_kernel(const int32_t* __restrict__ counts,
+                                                       const int32_t* __restrict__ offsets, int S, int64_t assignments,
+                                                       moe_balance_stats* out) {
+  __shared__ int32_t wmax[32];
+  const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+  const int c = e < S ? counts[e] : 0;
+  const int active = __syncthreads_count(c > 0);
+  int m = c;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) wmax[w] = m;
+  __syncthreads();
+  if (w == 0) {
+    m = wmax[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) {
+      const int kept = offsets[S];
+      out->max_rows = m;
+      out->active = active;
+      out->kept = kept;
+      out->dropped = (int32_t)(assignments - kept);
+      // max / (kept / S) = max * S / kept: exact in fp64 (both factors below 2^31 and 2^10), one division
+      out->max_over_mean = kept > 0 ? (float)((double)m * (double)S / (double)kept) : 0.f;
+    }
+  }
+}
+
 }  // namespace dp
+
+cudaError_t launch_balance(const int32_t* counts, const int32_t* offsets, int S, int64_t assignments,
+                           moe_balance_stats* out, cudaStream_t stream) {
+  dp::balance_kernel<<<1, 1024, 0, stream>>>(counts, offsets, S, assignments, out);
+  return cudaGetLastError();
+}
 
 int dispatch_blocks(int T) { return (int)cdiv(T, dp::TPB); }
 size_t dispatch_scratch_ints(int T, int E) { return (size_t)dispatch_blocks(T) * (size_t)E; }

@@ -6,6 +6,7 @@
 
 #include <string>
 
+#include "../../include/moe.h"
 #include "device_state.h"
 
 namespace moe {
@@ -80,6 +81,9 @@ struct DispatchDesc {
   int32_t* expert_counts = nullptr;  // scratch [E]: kept rows per logical expert
 };
 cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream);
+// Load balance of a step from its counts [S] and offsets [S + 1] (S <= 1024).
+cudaError_t launch_balance(const int32_t* counts, const int32_t* offsets, int S, int64_t assignments,
+                           moe_balance_stats* out, cudaStream_t stream);
 
 // Step 3: grouped GEMM (tcgen05) of one projection.
 struct GroupedGemmDesc {

@@ -86,6 +86,7 @@ def load():
                 "moe_graph_launch": [vp, vp],
                 "moe_graph_destroy": [vp],
                 "moe_eplb_plan": [vp, i32, i32, i32, vp, vp, vp, vp, vp],
+                "moe_balance": [cfgp, vp, vp, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -273,17 +274,18 @@ def selftest_wait_timeout(cfg, ws, limit_cycles: int) -> None:
 
 
 def balance(cfg, ws) -> dict:
-    """Load balance of the last step, read from its workspace (one small device-to-host copy): rows per
-    expert (per physical slot under a placement), busiest / mean (inference guide 6.4, section 5.1:
-    the step waits for the busiest expert), experts with rows, and the assignments a capacity limit
-    dropped."""
+    """Load balance of the last step, computed by the library (moe_balance) on the device from the
+    counts in its workspace and read back (one small copy): busiest expert's rows, busiest / mean
+    (inference guide 6.4, section 5.1: the step waits for the busiest expert), experts with rows, kept
+    rows, and the assignments a capacity limit dropped; plus the per-expert counts themselves (per
+    physical slot under a placement)."""
     S = cfg.placement.contents.n_slots if cfg.placement else cfg.E
+    stats = torch.zeros(8, dtype=torch.int32, device=ws.device)
+    _check(load().moe_balance(ctypes.byref(cfg), _ptr(ws), _ptr(stats), _stream()))
+    st = stats.cpu()
     counts = ws_view(ws, cfg, "counts", torch.int32, (S,)).cpu()
-    offsets = ws_view(ws, cfg, "offsets", torch.int32, (S + 1,)).cpu()
-    total = int(offsets[S])
-    mean = total / S if S else 0.0
-    return {"counts": counts.tolist(), "max_over_mean": (int(counts.max()) / mean) if mean > 0 else 0.0,
-            "active": int((counts > 0).sum()), "dropped": cfg.T * cfg.k - total}
+    return {"counts": counts.tolist(), "max_rows": int(st[0]), "active": int(st[1]), "kept": int(st[2]),
+            "dropped": int(st[3]), "max_over_mean": float(st[4:5].view(torch.float32)[0])}
 
 
 class MoeLayer:

@@ -39,11 +39,47 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def logit_tolerance(x_bits: np.ndarray, w_r: np.ndarray) -> np.ndarray:
-    """Allowed |logit error| per (token, expert) of an fp32-accumulated router GEMM: 2^-16 of
-    sum_d |x_d w_d| (the scale at which the accumulation rounds; the plain max|logit| is the wrong
-    scale when the terms cancel), computed by the oracle on the absolute values."""
-    return 2.0 ** -16 * oracle.router_logits(x_bits & np.uint16(0x7FFF), np.abs(w_r)).astype(np.float64) + 1e-6
+U32 = 2.0 ** -24  # unit roundoff of fp32 (round to nearest)
+
+
+def router_error_units(wl: synth.Workload) -> float:
+    """Worst-case error of the library's fp32 router GEMM, in units of U32 * sum_d |x_d w_d|.
+
+    Every product is exact: x is bf16 and the fp32 weight enters either as an fp32 FMA operand
+    (CUDA-core router) or split exactly into three bf16 terms (tensor-core router), and a bf16 x bf16
+    product has at most 16 significant bits. So all error comes from the additions, and by the
+    standard bound for summation (Higham, Accuracy and Stability of Numerical Algorithms, ch. 4) it is
+    at most D * delta * sum |terms|, where D is the longest chain of rounded additions a product passes
+    through and delta the relative error of one addition.
+
+    * CUDA-core router (E < 128, or E not a multiple of 32): delta = U32 (IEEE round to nearest). A
+      lane takes 8 elements of each 256-element K chunk of its warp's share, chunks split over kw
+      warps (kw = 8 when h / 256 >= 8, else 4, 2, 1), accumulated by fused multiply-adds: 8 *
+      ceil(chunks / kw) roundings; then a 5-level butterfly over the lanes and kw - 1 additions of
+      the warps' partial sums.
+    * Tensor-core router: the accumulator's internal rounding is not documented, so take the
+      pessimistic delta = 2 U32 (truncation) for every product added, as if the 512 products of a
+      TMEM chunk (8 K blocks of 64) were added one by one; the chunks (at most ceil(3 h / 512) per
+      tile) are summed in fp32 registers (round to nearest), and a split K range adds at most 128
+      partial sums in a fixed order.
+    """
+    if wl.E >= 128 and wl.E % 32 == 0:
+        return 2.0 * 512 + -(-3 * wl.h // 512) + 128
+    chunks = wl.h // 256
+    kw = 8 if chunks >= 8 else 4 if chunks >= 4 else 2 if chunks >= 2 else 1
+    return 8.0 * -(-chunks // kw) + 5 + (kw - 1)
+
+
+def router_abs_sum(x_bits: np.ndarray, w_r: np.ndarray) -> np.ndarray:
+    """sum_d |x_d w_d| per (token, expert), by the oracle on the absolute values."""
+    return oracle.router_logits(x_bits & np.uint16(0x7FFF), np.abs(w_r)).astype(np.float64)
+
+
+def logit_tolerance(wl: synth.Workload, x_bits: np.ndarray, w_r: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Allowed |GPU logit - oracle logit| per (token, expert): the router's worst-case error bound
+    (router_error_units) plus the half unit in the last place by which the oracle's own fp32 logit
+    (the exact sum, rounded once) can sit from the exact sum."""
+    return router_error_units(wl) * U32 * router_abs_sum(x_bits, w_r) + 0.5 * U32 * np.abs(ref) + 1e-30
 
 
 def rel_err_per_token(y_bits: np.ndarray, ref_bits_or_double: np.ndarray) -> np.ndarray:

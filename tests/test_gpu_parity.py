@@ -91,7 +91,7 @@ def _check_layer_against_oracle(wl, L: GpuLayer, min_clear=0.5):
 
     # step 1a: router GEMM against the fp64 oracle
     lo = oracle.router_logits(x, w_r)
-    assert np.all(np.abs(logits.astype(np.float64) - lo) <= logit_tolerance(x, w_r))
+    assert np.all(np.abs(logits.astype(np.float64) - lo) <= logit_tolerance(wl, x, w_r, lo))
 
     # the whole layer on identical logits
     ref = oracle.forward(x, w_r, bias, experts, shared, logits=logits, fp8=wl.dtype == "fp8",
@@ -465,6 +465,9 @@ def test_balance_stats_match_the_oracle_counts(cf):
     assert b["counts"] == counts.tolist()
     assert b["dropped"] == wl.T * wl.k - int(offsets[-1])
     assert b["active"] == int((counts > 0).sum())
-    assert b["max_over_mean"] == pytest.approx(counts.max() / (offsets[-1] / wl.E), rel=1e-12)
+    assert b["max_rows"] == int(counts.max())
+    assert b["kept"] == int(offsets[-1])
+    # busiest / mean, rounded once to fp32 by the library
+    assert b["max_over_mean"] == pytest.approx(counts.max() / (offsets[-1] / wl.E), rel=2.0 ** -24)
     if cf > 0:
         assert b["dropped"] > 0 and max(b["counts"]) <= cap  # the skewed router really overflows
