@@ -9,8 +9,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 SO = os.path.join(OUT_DIR, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "dispatch.cu", "gemm.cu", "gemm_pair.cu", "gemm_fp8.cu", "gemm_fp4.cu", "combine.cu", "eplb.cu"]
-HEADERS = ["common.cuh", "gemm_common.cuh", "kernels.h", "device_state.h"]
+SOURCES = ["api.cu", "route.cu", "dispatch.cu", "gemm.cu", "gemm_pair.cu", "gemm_fp8.cu", "gemm_fp4.cu", "combine.cu", "eplb.cu", "fused.cu"]
+HEADERS = ["common.cuh", "gemm_common.cuh", "kernels.h", "device_state.h", "route_impl.cuh", "dispatch_impl.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -134,8 +134,13 @@ int* status_ptr(void* ws, const moe_ws_layout& l) {
 // on the second stream. moe_forward zeroes them with the status word; moe_expert_ffn zeroes the
 // routed pair on its own stream.
 constexpr int kTileCounters = 4;
-static_assert((16 + kTileCounters) * sizeof(int) <= 256, "the scratch header holds the status word and the tile counters");
+// then the arrival counter of the fused small-batch kernel's grid barrier, also zeroed by moe_forward
+constexpr int kHeaderInts = 16 + kTileCounters + 1;
+static_assert(kHeaderInts * sizeof(int) <= 256, "the scratch header holds the status word and the counters");
 int* tile_ctr_ptr(void* ws, const moe_ws_layout& l) { return status_ptr(ws, l) + 16; }
+unsigned int* grid_barrier_ptr(void* ws, const moe_ws_layout& l) {
+  return reinterpret_cast<unsigned int*>(status_ptr(ws, l) + 16 + kTileCounters);
+}
 int32_t* hist_ptr(void* ws, const moe_ws_layout& l) {
   return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + l.scratch + 256);
 }
@@ -176,10 +181,12 @@ int check_ws(void* ws, size_t ws_bytes, const Layout& L) {
     if (!aligned16(p)) return fail(MOE_ERR_INVALID, std::string(name) + " must be 16-byte aligned"); \
   } while (0)
 
-int do_route(const moe_config* c, const void* x, const moe_weights* w, float* logits, int flags, int32_t* topk_idx,
-             float* topk_w, void* ws, const Layout& L, cudaStream_t stream) {
+// Step 1a, the router GEMM: logits = x W_r^T on the tensor cores (E >= 128, E % 32 == 0) or the
+// CUDA cores (otherwise).
+int do_router_gemm(const moe_config* c, const void* x, const moe_weights* w, float* logits, void* ws,
+                   const Layout& L, cudaStream_t stream) {
   cudaError_t e;
-  if (!(flags & MOE_LOGITS_GIVEN) && c->T > 0) {
+  if (c->T > 0) {
     if (tensor_core_router(c)) {
       void* w3 = at<void>(ws, L.l.router_w3);
       e = moe::launch_split_router_weight(w->w_router, w3, (int64_t)c->E * c->h, stream);
@@ -220,8 +227,13 @@ int do_route(const moe_config* c, const void* x, const moe_weights* w, float* lo
       counted(1);
     }
   }
+  return MOE_OK;
+}
+
+moe::TopkDesc topk_desc(const moe_config* c, const moe_weights* w, const float* logits, int32_t* topk_idx,
+                        float* topk_w) {
   moe::TopkDesc d;
-  d.logits = logits;
+  d.logits = const_cast<float*>(logits);
   d.bias = w ? w->bias : nullptr;
   d.topk_idx = topk_idx;
   d.topk_w = topk_w;
@@ -234,7 +246,16 @@ int do_route(const moe_config* c, const void* x, const moe_weights* w, float* lo
   d.renorm = c->renormalize;
   d.routed_scale = c->routed_scale;
   if (c->score == MOE_SCORE_SOFTMAX) d.bias = nullptr;
-  e = moe::launch_topk(d, stream);
+  return d;
+}
+
+int do_route(const moe_config* c, const void* x, const moe_weights* w, float* logits, int flags, int32_t* topk_idx,
+             float* topk_w, void* ws, const Layout& L, cudaStream_t stream) {
+  if (!(flags & MOE_LOGITS_GIVEN)) {
+    const int rc = do_router_gemm(c, x, w, logits, ws, L, stream);
+    if (rc) return rc;
+  }
+  cudaError_t e = moe::launch_topk(topk_desc(c, w, logits, topk_idx, topk_w), stream);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   if (c->T > 0) counted(1);
   return MOE_OK;
@@ -274,6 +295,45 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   cudaError_t e = moe::launch_dispatch(d, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   if (c->T > 0) counted(4);
+  return MOE_OK;
+}
+
+// Small batches in moe_forward: router (E < 128), top-k, counts, offsets, rows and the dispatch copy as
+// one cooperative kernel instead of six launches (Perplexity "CUDA Graph"; TensorRT-LLM "Runtime
+// optimizations": a decode step is launch-bound). Dropless layers with one slot per expert only.
+bool use_fused(const moe_config* c) {
+  return moe::fused_route_dispatch_supported(c->T, c->E) && capacity_of(c) == 0 && !c->placement;
+}
+
+int do_fused_route_dispatch(const moe_config* c, const void* x, const moe_weights* w, void* ws, const Layout& L,
+                            cudaStream_t stream, bool shared_rows) {
+  const moe_ws_layout& l = L.l;
+  float* logits = at<float>(ws, l.logits);
+  const bool tc = tensor_core_router(c);
+  if (tc) {
+    const int rc = do_router_gemm(c, x, w, logits, ws, L, stream);
+    if (rc) return rc;
+  }
+  moe::FusedRouteDispatchDesc d;
+  d.x = x;
+  d.w_router = w->w_router;
+  d.run_router = tc ? 0 : 1;
+  d.tk = topk_desc(c, w, logits, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w));
+  d.counts = at<int32_t>(ws, l.counts);
+  d.offsets = at<int32_t>(ws, l.offsets);
+  d.inv_pos = at<int32_t>(ws, l.inv_pos);
+  d.row_token = at<int32_t>(ws, l.row_token);
+  d.row_weight = at<float>(ws, l.row_weight);
+  d.xd = at<void>(ws, l.xd);
+  d.xd_scales = at<float>(ws, l.xd_scales);
+  d.h = c->h;
+  d.shared = c->I_shared > 0 && shared_rows;
+  d.fp8 = c->dtype == MOE_DTYPE_FP8_BLOCK128;
+  d.barrier = grid_barrier_ptr(ws, l);
+  d.status = status_ptr(ws, l);
+  cudaError_t e = moe::launch_fused_route_dispatch(d, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused route-and-dispatch launch");
+  counted(1);
   return MOE_OK;
 }
 
@@ -656,16 +716,22 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
   REQUIRE_PTR(weights->w_router, "weights->w_router");
   if ((rc = check_expert_weights(cfg, weights))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  // the status word and the grouped GEMMs' tile counters
-  cudaError_t e = cudaMemsetAsync(status_ptr(ws, L.l), 0, (16 + kTileCounters) * sizeof(int), s);
+  // the status word, the grouped GEMMs' tile counters and the fused kernel's barrier counter
+  cudaError_t e = cudaMemsetAsync(status_ptr(ws, L.l), 0, kHeaderInts * sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "status reset");
   const moe_ws_layout& l = L.l;
-  if ((rc = do_route(cfg, x, weights, at<float>(ws, l.logits), 0, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w),
-                     ws, L, s)))
-    return rc;
-  // bf16 layers with a shared expert: the shared expert runs on a second stream from here on (it
-  // needs only x), overlapping dispatch and the routed GEMMs; the combine waits for it
+  // bf16 layers with a shared expert: the shared expert runs on a second stream (it needs only x),
+  // overlapping dispatch and the routed GEMMs; the combine waits for it
   const bool side = cfg->I_shared > 0 && cfg->T > 0 && cfg->dtype == MOE_DTYPE_BF16;
+  // small batches: routing and dispatch as one cooperative kernel, before the second stream forks (the
+  // fork then overlaps the routed GEMMs, and the cooperative grid never shares the SMs with it)
+  const bool fused = use_fused(cfg);
+  if (fused) {
+    if ((rc = do_fused_route_dispatch(cfg, x, weights, ws, L, s, !side))) return rc;
+  } else if ((rc = do_route(cfg, x, weights, at<float>(ws, l.logits), 0, at<int32_t>(ws, l.topk_idx),
+                            at<float>(ws, l.topk_w), ws, L, s))) {
+    return rc;
+  }
   std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
   SideStream side_handles;
   SideStream* sd = &side_handles;
@@ -682,10 +748,10 @@ MOE_EXPORT int moe_forward(const moe_config* cfg, const void* x, const moe_weigh
       return src;
     }
   }
-  if ((rc = do_dispatch(cfg, x, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w), at<int32_t>(ws, l.counts),
-                        at<int32_t>(ws, l.offsets), at<int32_t>(ws, l.inv_pos), at<int32_t>(ws, l.row_token),
-                        at<float>(ws, l.row_weight), at<void>(ws, l.xd), at<float>(ws, l.xd_scales), ws, L, s,
-                        !side))) {
+  if (!fused && (rc = do_dispatch(cfg, x, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w),
+                                  at<int32_t>(ws, l.counts), at<int32_t>(ws, l.offsets), at<int32_t>(ws, l.inv_pos),
+                                  at<int32_t>(ws, l.row_token), at<float>(ws, l.row_weight), at<void>(ws, l.xd),
+                                  at<float>(ws, l.xd_scales), ws, L, s, !side))) {
     if (side) cudaStreamWaitEvent(s, sd->join, 0);
     return rc;
   }

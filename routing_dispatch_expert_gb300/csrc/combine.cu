@@ -60,22 +60,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 }
 
 // k <= KMAX: all k (+1 shared) rows of a 256-element chunk are loaded before any is added, so a warp
-// keeps k + 1 independent 16-byte loads per lane in flight; the sum is still taken in slot order.
+// keeps k + 1 independent 16-byte loads per lane in flight; the sum is still taken in slot order. The
+// unit of work is one warp on PIECE consecutive 256-element chunks of one token's row, so that a batch
+// of few tokens (decode) still spreads over every SM.
+constexpr int PIECE = 4;
 template <int KMAX>
 __global__ void __launch_bounds__(256) combine_small_k_kernel(const uint4* __restrict__ yd,
                                                               const int32_t* __restrict__ inv_pos,
                                                               uint4* __restrict__ y, int T, int h, int k, int R,
                                                               int shared) {
   const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int64_t warps = (gridDim.x * blockDim.x) >> 5;
   const int hv = h / 8;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+  const int per = (hv / 32 + PIECE - 1) / PIECE;  // pieces per row (h is a multiple of 256)
+  for (int64_t it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < (int64_t)T * per; it += warps) {
+    const int t = (int)(it / per);
+    const int c_lo = (int)(it - (int64_t)t * per) * PIECE * 32;
+    const int c_hi = min(hv, c_lo + PIECE * 32);
     const int my_row = lane < k ? inv_pos[(int64_t)t * k + lane] : -1;
     int rows[KMAX + 1];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) rows[j] = __shfl_sync(0xffffffffu, my_row, j);  // -1 past k
     rows[KMAX] = shared ? R + t : -1;
-    for (int c = lane; c < hv; c += 32) {
+    for (int c = c_lo + lane; c < c_hi; c += 32) {
       uint4 v[KMAX + 1];
 #pragma unroll
       for (int j = 0; j <= KMAX; ++j)
@@ -149,7 +156,9 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(const uint4* __res
 cudaError_t launch_combine(const void* yd, const int32_t* inv_pos, void* y, int T, int h, int k, int shared,
                            cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  int64_t blocks = cdiv(T, 8);
+  // small k: one warp per piece of a row; larger k: one warp per token
+  const int64_t units = k <= 8 ? (int64_t)T * ((h / 256 + cb::PIECE - 1) / cb::PIECE) : T;
+  int64_t blocks = cdiv(units, 8);
   if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
   if (k <= 8)
     cb::combine_small_k_kernel<8><<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(yd), inv_pos,

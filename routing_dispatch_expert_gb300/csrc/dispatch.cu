@@ -13,11 +13,13 @@
 //   3. rank        per 512-token block: per-warp lane masks of each expert give every (token, slot)
 //                  its row, rows of an expert in ascending token order -> inv_pos, row_token,
 //                  row_weight
-//   4. gather      one warp per token: the token's row is read once and written to its k rows
-//                  (and to the shared expert's row), as bf16 or as e4m3 with 1x128 scales.
+//   4. gather      one warp per item (a 1024-element piece of one token's row): the piece is read
+//                  once and written to the token's k rows (and to the shared expert's row), as bf16
+//                  or as e4m3 with 1x128 scales (dispatch_impl.cuh).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "dispatch_impl.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -160,84 +162,25 @@ __global__ void __launch_bounds__(TPB) rank_kernel(const int32_t* __restrict__ i
   }
 }
 
-// one warp per token; lane covers 8 consecutive elements of every 256-element chunk
+// The dispatch copies: one warp per item (a piece of one token's row), items in token order.
 __global__ void __launch_bounds__(256) gather_bf16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_pos,
                                                           uint4* __restrict__ xd, int T, int h, int k, int R,
                                                           int shared) {
   const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int hv = h / 8;  // uint4 per row
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const int my_row = lane < k ? inv_pos[(int64_t)t * k + lane] : -1;
-    const uint4* src = x + (int64_t)t * hv;
-    for (int c = lane; c < hv; c += 128) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c + 32 * u < hv) v[u] = src[c + 32 * u];
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, my_row, j);
-        if (r < 0) continue;
-        uint4* dst = xd + (int64_t)r * hv;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (c + 32 * u < hv) dst[c + 32 * u] = v[u];
-      }
-      if (shared) {
-        uint4* dst = xd + (int64_t)(R + t) * hv;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (c + 32 * u < hv) dst[c + 32 * u] = v[u];
-      }
-    }
-  }
+  const int64_t warps = (gridDim.x * blockDim.x) >> 5;
+  const int64_t items = (int64_t)T * bf16_items_per_row(h);
+  for (int64_t it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += warps)
+    gather_bf16_item(x, inv_pos, xd, h, k, R, shared, it, lane);
 }
 
-// FP8 variant: every 128-element block is quantised once (amax over 16 lanes), then its codes and
-// scale are written to the token's k rows (and the shared expert's row).
 __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_pos,
                                                          uint8_t* __restrict__ xd, float* __restrict__ xs, int T, int h,
                                                          int k, int R, int shared) {
   const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int hv = h / 8;
-  const int hb = h / 128;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const int my_row = lane < k ? inv_pos[(int64_t)t * k + lane] : -1;
-    const uint4* src = x + (int64_t)t * hv;
-    for (int c = lane; c < hv; c += 32) {  // 256 elements per pass: lanes 0-15 one block, 16-31 the next
-      uint4 v = src[c];
-      float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                    bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-      uint32_t q[2] = {0, 0};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t code = __nv_cvt_float_to_fp8(__fdiv_rn(f[i], scale), __NV_SATFINITE, __NV_E4M3);
-        q[i / 4] |= code << (8 * (i % 4));
-      }
-      const uint2 qv = make_uint2(q[0], q[1]);
-      const int blk = (c * 8) / 128;
-      const bool scale_writer = (lane & 15) == 0;
-      for (int j = 0; j <= k; ++j) {
-        int r;
-        if (j < k) {
-          r = __shfl_sync(0xffffffffu, my_row, j);
-          if (r < 0) continue;
-        } else {
-          if (!shared) break;
-          r = R + t;
-        }
-        *reinterpret_cast<uint2*>(xd + (int64_t)r * h + c * 8) = qv;
-        if (scale_writer) xs[(int64_t)r * hb + blk] = scale;
-      }
-    }
-  }
+  const int64_t warps = (gridDim.x * blockDim.x) >> 5;
+  const int64_t items = (int64_t)T * fp8_items_per_row(h);
+  for (int64_t it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += warps)
+    gather_fp8_item(x, inv_pos, xd, xs, h, k, R, shared, it, lane);
 }
 
 // Load balance of one step from its counts (S <= 1024 experts or slots): the busiest expert's rows,
@@ -311,7 +254,8 @@ cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream) {
   dp::rank_kernel<<<nblk, dp::TPB, rank_smem, stream>>>(d.topk_idx, d.topk_w, d.scratch, d.offsets, d.T, d.k, d.E,
                                                          cap, d.inv_pos, d.row_token, d.row_weight, d.n_slots,
                                                          d.max_replicas, d.replicas, d.replica_slot);
-  int64_t blocks = cdiv(d.T, 8);
+  const int64_t items = (int64_t)d.T * (d.fp8 ? dp::fp8_items_per_row(d.h) : dp::bf16_items_per_row(d.h));
+  int64_t blocks = cdiv(items, 8);
   if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
   const int R = d.T * d.k;
   if (d.fp8)

@@ -7,8 +7,8 @@ The sample (SURVEY: a seeded sample of at least 2048 tokens for the FFN and comb
 seeded random tokens plus forced ones: for every expert with rows, the tokens of the first and last
 row of its last 128-row tile (the ragged tail a grouped GEMM tile covers only partly, which the
 CTA-pair kernel runs as a half tile), and for the four busiest experts 64 tokens spread over their
-rows (the long groups the tile scheduler walks in bands). The decode layers (256 tokens) are checked
-on every token."""
+rows (the long groups the tile scheduler walks in bands). The tiny layer (4096 tokens) and the decode
+layers (256 tokens) are checked on every token."""
 import gc
 
 import numpy as np
@@ -61,7 +61,7 @@ def _rel_rows(got, ref):
     return np.abs(got - ref).max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-30)
 
 
-@pytest.mark.parametrize("name,n_tok", [("mixtral", 2048), ("dsv3_prefill", 2048), ("dsv3_decode", None),
+@pytest.mark.parametrize("name,n_tok", [("tiny", None), ("mixtral", 2048), ("dsv3_prefill", 2048), ("dsv3_decode", None),
                                         ("dsv3_fp8", 2048), ("dsv3_decode_fp4", None)])
 def test_full_size_layer(name, n_tok):
     wl = synth.WORKLOADS[name]
