@@ -70,7 +70,6 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* ctr, int n, int* stat
         ok = 0;
         break;
       }
-      __nanosleep(64);
     }
     __threadfence();
     ok_s = ok;
@@ -161,13 +160,31 @@ __global__ void __launch_bounds__(THREADS, 1) route_dispatch_kernel(const Args a
   __syncthreads();
   const int32_t* idx = a.tk.topk_idx;
   bool bad = false;
-  for (int64_t i = threadIdx.x; i < (int64_t)T * k; i += THREADS) {
-    const int e = __ldcg(idx + i);
-    if (e >= 0 && e < E) {
-      atomicAdd(&cnt[e], 1);
-      if (i < (int64_t)t0 * k) atomicAdd(&before[e], 1);
-    } else if (i >= (int64_t)t0 * k && i < (int64_t)t1 * k) {
-      bad = true;
+  {
+    // UNROLL indices per thread in flight, then one shared-memory atomic per distinct expert of a warp
+    // (lanes holding the same expert add together)
+    constexpr int UNROLL = 8;
+    const int64_t n = (int64_t)T * k, n_before = (int64_t)t0 * k, own_end = (int64_t)t1 * k;
+    for (int64_t i0 = 0; i0 < n; i0 += (int64_t)THREADS * UNROLL) {
+      int ev[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int64_t i = i0 + (int64_t)u * THREADS + threadIdx.x;
+        ev[u] = i < n ? __ldcg(idx + i) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int64_t i = i0 + (int64_t)u * THREADS + threadIdx.x;
+        const bool in = i < n;
+        const int e = ev[u];
+        const bool ok = in && e >= 0 && e < E;
+        if (in && !ok && i >= n_before && i < own_end) bad = true;
+        const bool pre = ok && i < n_before;
+        const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
+        const unsigned grp_pre = __match_any_sync(0xffffffffu, pre ? e : -1);
+        if (ok && (__ffs(grp) - 1) == lane) atomicAdd(&cnt[e], __popc(grp));
+        if (pre && (__ffs(grp_pre) - 1) == lane) atomicAdd(&before[e], __popc(grp_pre));
+      }
     }
   }
   if (bad) atomicOr(a.status, MOE_STATUS_BAD_EXPERT_INDEX);

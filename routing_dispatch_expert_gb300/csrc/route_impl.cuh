@@ -146,12 +146,15 @@ struct Slots {
 
 // Group stage and expert stage on the keys of one token. Returns in sel_e / sel_l (lanes < k) the
 // chosen experts in descending key order and their logits. *clear is false when a deciding gap is
-// below the thresholds (only tracked when track_gaps).
+// below the thresholds (only tracked when track_gaps); *groups_clear is false when the group stage's
+// gap is, and *cut is the best key left out of the selection (the (k+1)-th, when track_gaps).
 template <int EPL>
 __device__ __forceinline__ void select_experts(const TopkDesc& d, const Slots<EPL>& sl, const float (&key)[EPL],
                                                const float (&lv)[EPL], int lane, bool track_gaps, int& sel_e,
-                                               float& sel_l, bool& clear) {
+                                               float& sel_l, bool& clear, bool& groups_clear, float& cut) {
   clear = true;
+  groups_clear = true;
+  cut = -INFINITY;
   uint32_t kept = 0xffffffffu;
   if (d.n_group > 1) {
     // the score of group g (sum of its two best keys) ends in every lane of the group (lane-aligned
@@ -224,7 +227,7 @@ __device__ __forceinline__ void select_experts(const TopkDesc& d, const Slots<EP
       const bool out = my_group >= 0 && !((kept >> my_group) & 1u);
       const float kept_min = unord(__reduce_min_sync(0xffffffffu, in ? gu : 0xffffffffu));
       const float rest_max = unord(__reduce_max_sync(0xffffffffu, out ? gu : 0u));
-      if (!(kept_min - rest_max > kGroupGap)) clear = false;
+      if (!(kept_min - rest_max > kGroupGap)) clear = groups_clear = false;
     }
   }
   uint32_t uk[EPL];
@@ -250,7 +253,10 @@ __device__ __forceinline__ void select_experts(const TopkDesc& d, const Slots<EP
     const float bv = unord(m);
     if (track_gaps && j > 0 && !(prev - bv > kKeyGap)) clear = false;
     prev = bv;
-    if (j == d.k) break;  // the (k+1)-th key only checks the gap
+    if (j == d.k) {  // the (k+1)-th key only checks the gap
+      cut = bv;
+      break;
+    }
     const uint32_t b = __ballot_sync(0xffffffffu, m != 0 && lb == m);
     const int wl = b ? __ffs(b) - 1 : 0;
     const int wi = __shfl_sync(0xffffffffu, li, wl);
@@ -315,62 +321,94 @@ __device__ __forceinline__ void topk_token(const TopkDesc& d, const Slots<EPL>& 
   }
   int sel_e;
   float sel_l;
-  bool clear;
-  select_experts<EPL>(d, sl, key, lv, lane, sigmoid, sel_e, sel_l, clear);
+  bool clear, groups_clear;
+  float cut;
+  select_experts<EPL>(d, sl, key, lv, lane, sigmoid, sel_e, sel_l, clear, groups_clear, cut);
   if (sigmoid && !clear) {
-    // a near tie: decide on the exact keys
+    // A near tie: decide on the exact keys (fp64 sigmoid, slow on this part's fp64 pipe). When the
+    // group stage is settled (its gap exceeds twice the fast keys' error, so the same groups are kept
+    // on exact keys), only an expert whose fast key lies within kCutWindow of the best key left out
+    // can enter the selection or change its order: every other key stays more than kCutWindow - 2 x
+    // 4e-7 away from each re-evaluated one, so its order against them is the same on exact keys.
+    // Those experts keep their fast keys; slot positions no lane needs are skipped. With a group near
+    // tie every key is re-evaluated.
+    constexpr float kCutWindow = 2e-6f;
+    const float lo = groups_clear ? cut - kCutWindow : -INFINITY;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      float kv = __fadd_rn(sigmoid_exact(lv[i]), sl.bias[i]);
-      if (kv != kv) kv = -INFINITY;
-      key[i] = sl.valid[i] ? kv : -INFINITY;
+      const bool need = sl.valid[i] && key[i] >= lo;
+      if (__any_sync(0xffffffffu, need) && need) {
+        float kv = __fadd_rn(sigmoid_exact(lv[i]), sl.bias[i]);
+        if (kv != kv) kv = -INFINITY;
+        key[i] = kv;
+      }
     }
-    select_experts<EPL>(d, sl, key, lv, lane, false, sel_e, sel_l, clear);
+    select_experts<EPL>(d, sl, key, lv, lane, false, sel_e, sel_l, clear, groups_clear, cut);
   }
 
-  // route weights
-  double w = 0.0;
+  // route weights. They enter the combine, not a selection, so they are formed in fp32 (this part's
+  // fp64 pipe runs at a small fraction of the fp32 rate, and a few fp64 operations per token made the
+  // whole top-k fp64-bound), with error bounds well inside the weights' tolerance:
   if (sigmoid) {
-    // w_j = s_j / sum(s) * scale with s = sigmoid(logit) in fp32 (relative error below 4e-7), the
-    // sum of the k scores in fp64; the weights enter the combine, not a selection, so they need no
-    // correctly rounded sigmoid
+    // w_j = s_j * (scale / sum s): s in fp32 (relative error below 4e-7); the k scores summed in slot
+    // order by every lane (the same sum on every lane, k - 1 roundings)
     const float sj = lane < d.k ? sigmoid_fast(sel_l) : 0.f;
-    double sum = (double)sj;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float scale = d.renorm ? __fdiv_rn(d.routed_scale, (float)sum) : d.routed_scale;
+    float sum = 0.f;
+    for (int j = 0; j < d.k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, sj, j));
+    const float scale = d.renorm ? __fdiv_rn(d.routed_scale, sum) : d.routed_scale;
     if (lane < d.k) {
       d.topk_idx[(int64_t)t * d.k + lane] = sel_e;
       d.topk_w[(int64_t)t * d.k + lane] = __fmul_rn(sj, scale);
     }
     return;
   }
-  {
-    // softmax probabilities: the exponentials in fp32 (at most 2 ulp, relative error below 3e-7
-    // with the rounding of l - lmax), summed and divided in fp64; the probabilities enter the
-    // combine, not a selection (fp64 exp costs ~15 us per launch on this part's slow fp64 pipe)
-    float lmax = -INFINITY;
+  // softmax: e_i = exp(l_i - lmax), with the rounding error of the subtraction carried into the
+  // exponential (l - lmax = dh + dl exactly, e = expf(dh) * (1 + dl)), so e has expf's 2 ulp plus a
+  // few roundings. Renormalised, w_j = e_j / sum_sel e (the normaliser over all experts cancels; k - 1
+  // roundings in slot order); otherwise w_j = e_j / z with z = sum over all experts, per lane in slot
+  // order and then a butterfly (every lane ends with the same z; EPL + 4 roundings); above 256
+  // experts z is summed in fp64 to keep its error small.
+  float lmax = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (sl.valid[i]) lmax = fmaxf(lmax, lv[i]);
+  lmax = warp_max(lmax);
+  auto expd = [lmax](float l) {
+    const float b = -lmax;
+    const float dh = __fadd_rn(l, b);
+    const float e = expf(dh);
+    if (!(e > 0.f) || isinf(e)) return e;  // 0, inf or NaN: nothing to correct
+    // TwoSum (Knuth): dh + dl == l + b exactly
+    const float bb = __fsub_rn(dh, l);
+    const float dl = __fadd_rn(__fsub_rn(l, __fsub_rn(dh, bb)), __fsub_rn(b, bb));
+    return __fmaf_rn(e, dl, e);  // exp(dh + dl) to first order in dl (|dl| <= 2^-24 |dh|)
+  };
+  const float e_sel = lane < d.k ? expd(sel_l) : 0.f;
+  float w;
+  if (d.renorm) {
+    float sum = 0.f;
+    for (int j = 0; j < d.k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, e_sel, j));
+    w = __fdiv_rn(e_sel, sum);
+  } else if (EPL <= 8) {
+    float z = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
-      if (sl.valid[i]) lmax = fmaxf(lmax, lv[i]);
-    lmax = warp_max(lmax);
+      if (sl.valid[i]) z = __fadd_rn(z, expd(lv[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xffffffffu, z, o));
+    w = __fdiv_rn(e_sel, z);
+  } else {
     double z = 0.0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
-      if (sl.valid[i]) z += (double)expf(lv[i] - lmax);
+      if (sl.valid[i]) z += (double)expd(lv[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane < d.k) w = (double)expf(sel_l - lmax) / z;
-  }
-  if (d.renorm) {
-    double sum = lane < d.k ? w : 0.0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    w = w / sum;
+    w = (float)((double)e_sel / z);
   }
   if (lane < d.k) {
     d.topk_idx[(int64_t)t * d.k + lane] = sel_e;
-    d.topk_w[(int64_t)t * d.k + lane] = (float)(w * (double)d.routed_scale);
+    d.topk_w[(int64_t)t * d.k + lane] = __fmul_rn(w, d.routed_scale);
   }
 }
 
