@@ -298,26 +298,25 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
   return MOE_OK;
 }
 
-// Small batches in moe_forward: router (E < 128), top-k, counts, offsets, rows and the dispatch copy as
-// one cooperative kernel instead of six launches (Perplexity "CUDA Graph"; TensorRT-LLM "Runtime
-// optimizations": a decode step is launch-bound). Dropless layers with one slot per expert only.
+// Small batches in moe_forward: router, top-k, counts, offsets, rows and the dispatch copy as one
+// cooperative kernel instead of six launches (Perplexity "CUDA Graph"; TensorRT-LLM "Runtime
+// optimizations": a small step is launch-bound). Used where the router runs on the CUDA cores (E < 128,
+// or E not a multiple of 32): with the tensor-core router in front, the fused kernel would replace
+// only five short launches, and measured slower than them (a 256-token decode step: about 46 us
+// against about 30 us, its phases separated by grid barriers and its top-k latency-bound on the few
+// tokens). Dropless layers with one slot per expert only.
 bool use_fused(const moe_config* c) {
-  return moe::fused_route_dispatch_supported(c->T, c->E) && capacity_of(c) == 0 && !c->placement;
+  return moe::fused_route_dispatch_supported(c->T, c->E) && capacity_of(c) == 0 && !c->placement &&
+         !tensor_core_router(c);
 }
 
 int do_fused_route_dispatch(const moe_config* c, const void* x, const moe_weights* w, void* ws, const Layout& L,
                             cudaStream_t stream, bool shared_rows) {
   const moe_ws_layout& l = L.l;
   float* logits = at<float>(ws, l.logits);
-  const bool tc = tensor_core_router(c);
-  if (tc) {
-    const int rc = do_router_gemm(c, x, w, logits, ws, L, stream);
-    if (rc) return rc;
-  }
   moe::FusedRouteDispatchDesc d;
   d.x = x;
   d.w_router = w->w_router;
-  d.run_router = tc ? 0 : 1;
   d.tk = topk_desc(c, w, logits, at<int32_t>(ws, l.topk_idx), at<float>(ws, l.topk_w));
   d.counts = at<int32_t>(ws, l.counts);
   d.offsets = at<int32_t>(ws, l.offsets);

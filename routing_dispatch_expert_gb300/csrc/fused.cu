@@ -3,12 +3,12 @@
 // Perplexity blog "Lower latency and higher throughput with multi-node DeepSeek deployment", "CUDA
 // Graph", and TensorRT-LLM "DeepSeek R1 throughput on Blackwell", "Runtime optimizations": a decode
 // step is bound by the number of kernel launches, not by its work, so its many small kernels are to be
-// merged into few fixed-grid ones. For a batch of at most kFusedMaxT tokens the router GEMM (small E,
-// CUDA cores), the top-k selection, the per-expert counts and offsets, the stable expert-major row of
-// every (token, slot) and the dispatch copy run as one cooperative launch of one CTA per SM, in phases
-// separated by a grid-wide barrier:
-//   0  router logits (when E < 128: the same work units as router_small_e_kernel, two per CTA)
-//   1  top-k of every token, one warp per token (the same function as topk_kernel)
+// merged into few fixed-grid ones. For a batch of at most kFusedMaxT tokens of a layer whose router runs
+// on the CUDA cores (E < 128, or E not a multiple of 32), the router GEMM, the top-k selection, the
+// per-expert counts and offsets, the stable expert-major row of every (token, slot) and the dispatch
+// copy run as one cooperative launch of one CTA per SM, in phases separated by a grid-wide barrier:
+//   0  router logits (the same work units as router_small_e_kernel, two per CTA)
+//   1  top-k of every token, one warp per token spread over the SMs (the same function as topk_kernel)
 //   2  every CTA counts the experts of all T*k assignments, and separately of the tokens before its own
 //      range, in shared memory; scans the counts into offsets (CTA 0 stores counts and offsets); and
 //      places the assignments of its own tokens: row = offsets[e] + (earlier tokens choosing e), the
@@ -33,7 +33,6 @@ constexpr int PART_FLOATS = 512;  // router partial sums of one 256-thread unit 
 struct Args {
   const __nv_bfloat16* x;
   const float* w_router;
-  int run_router;  // 0: logits are given (tensor-core router ran before)
   int rg_emax, rg_kw;
   TopkDesc tk;
   int32_t* counts;
@@ -130,7 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1) route_dispatch_kernel(const Args a
   int nbar = 0;
 
   // ---- phase 0: router logits
-  if (a.run_router) {
+  {
     float* part_all = reinterpret_cast<float*>(smem);
     switch (a.rg_emax) {
       case 8: router_phase<8, 4>(a, part_all); break;
@@ -138,13 +137,14 @@ __global__ void __launch_bounds__(THREADS, 1) route_dispatch_kernel(const Args a
       case 32: router_phase<32, 1>(a, part_all); break;
       default: router_phase<64, 1>(a, part_all); break;
     }
-    if (!grid_barrier(a.barrier, nbar++, a.status, a.wait_limit)) return;
   }
+  if (!grid_barrier(a.barrier, nbar++, a.status, a.wait_limit)) return;
 
-  // ---- phase 1: top-k, one warp per token
+  // ---- phase 1: top-k, one warp per token, consecutive tokens on different SMs (a token's selection is
+  // a long chain of dependent warp operations, so a small batch finishes sooner with few warps per SM)
   {
     const tk::Slots<EPL> sl = tk::make_slots<EPL>(a.tk, lane);
-    for (int t = blockIdx.x * WARPS + warp; t < T; t += gridDim.x * WARPS) tk::topk_token<EPL>(a.tk, sl, lane, t);
+    for (int t = warp * gridDim.x + blockIdx.x; t < T; t += gridDim.x * WARPS) tk::topk_token<EPL>(a.tk, sl, lane, t);
   }
   if (!grid_barrier(a.barrier, nbar++, a.status, a.wait_limit)) return;
 
@@ -160,31 +160,13 @@ __global__ void __launch_bounds__(THREADS, 1) route_dispatch_kernel(const Args a
   __syncthreads();
   const int32_t* idx = a.tk.topk_idx;
   bool bad = false;
-  {
-    // UNROLL indices per thread in flight, then one shared-memory atomic per distinct expert of a warp
-    // (lanes holding the same expert add together)
-    constexpr int UNROLL = 8;
-    const int64_t n = (int64_t)T * k, n_before = (int64_t)t0 * k, own_end = (int64_t)t1 * k;
-    for (int64_t i0 = 0; i0 < n; i0 += (int64_t)THREADS * UNROLL) {
-      int ev[UNROLL];
-#pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
-        const int64_t i = i0 + (int64_t)u * THREADS + threadIdx.x;
-        ev[u] = i < n ? __ldcg(idx + i) : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
-        const int64_t i = i0 + (int64_t)u * THREADS + threadIdx.x;
-        const bool in = i < n;
-        const int e = ev[u];
-        const bool ok = in && e >= 0 && e < E;
-        if (in && !ok && i >= n_before && i < own_end) bad = true;
-        const bool pre = ok && i < n_before;
-        const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1);
-        const unsigned grp_pre = __match_any_sync(0xffffffffu, pre ? e : -1);
-        if (ok && (__ffs(grp) - 1) == lane) atomicAdd(&cnt[e], __popc(grp));
-        if (pre && (__ffs(grp_pre) - 1) == lane) atomicAdd(&before[e], __popc(grp_pre));
-      }
+  for (int64_t i = threadIdx.x; i < (int64_t)T * k; i += THREADS) {
+    const int e = __ldcg(idx + i);
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[e], 1);
+      if (i < (int64_t)t0 * k) atomicAdd(&before[e], 1);
+    } else if (i >= (int64_t)t0 * k && i < (int64_t)t1 * k) {
+      bad = true;
     }
   }
   if (bad) atomicOr(a.status, MOE_STATUS_BAD_EXPERT_INDEX);
@@ -287,7 +269,6 @@ cudaError_t launch_fused_route_dispatch(const FusedRouteDispatchDesc& d, cudaStr
   fz::Args a;
   a.x = reinterpret_cast<const __nv_bfloat16*>(d.x);
   a.w_router = d.w_router;
-  a.run_router = d.run_router;
   const int chunks = d.h / 256;
   a.rg_kw = chunks >= rg::WARPS ? rg::WARPS : chunks >= 4 ? 4 : chunks >= 2 ? 2 : 1;
   a.rg_emax = d.tk.E <= 8 ? 8 : d.tk.E <= 16 ? 16 : d.tk.E <= 32 ? 32 : 64;

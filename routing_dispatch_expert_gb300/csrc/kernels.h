@@ -81,16 +81,15 @@ struct DispatchDesc {
   int32_t* expert_counts = nullptr;  // scratch [E]: kept rows per logical expert
 };
 cudaError_t launch_dispatch(const DispatchDesc& d, cudaStream_t stream);
-// Steps 1-3 of a small batch as one cooperative launch (fused.cu): the router GEMM when run_router
-// (E < 128 on the CUDA cores; otherwise the logits come from the tensor-core router), top-k, counts,
-// offsets, rows and the dispatch copy. Dropless, one slot per expert, T <= kFusedMaxT, E <= 256.
+// Steps 1-3 of a small batch as one cooperative launch (fused.cu): the router GEMM on the CUDA cores
+// (E < 128, or E not a multiple of 32), top-k, counts, offsets, rows and the dispatch copy. Dropless,
+// one slot per expert, T <= kFusedMaxT, E <= 256.
 constexpr int kFusedMaxT = 4096;
 bool fused_route_dispatch_supported(int T, int E);
 struct FusedRouteDispatchDesc {
   const void* x;
   const float* w_router;
-  int run_router;
-  TopkDesc tk;  // logits (out when run_router, else in), bias, topk_idx, topk_w and the routing shape
+  TopkDesc tk;  // logits (out), bias, topk_idx, topk_w and the routing shape
   int32_t* counts;
   int32_t* offsets;
   int32_t* inv_pos;

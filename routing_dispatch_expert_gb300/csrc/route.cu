@@ -87,7 +87,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const TopkDesc d) {
 
 cudaError_t launch_topk(const TopkDesc& d, cudaStream_t stream) {
   if (d.T == 0) return cudaSuccess;
-  const int threads = 256;
+  // a token's selection is a long chain of dependent warp operations: a small batch spreads its tokens
+  // over the SMs two warps per CTA (few warps per SM, each issuing at a full sub-partition's rate), a
+  // large one packs eight warps per CTA
+  const int threads = d.T <= 8192 ? 64 : 256;
   int64_t blocks = cdiv(d.T, threads / 32);
   if (blocks > (int64_t)num_sms() * 16) blocks = (int64_t)num_sms() * 16;
   const int epl = (d.E + 31) / 32;

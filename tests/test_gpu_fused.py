@@ -1,5 +1,6 @@
-"""The small-batch path of moe_forward: for T <= 4096 (dropless, one slot per expert) the router
-(E < 128), top-k, counts, offsets, rows and the dispatch copy run as one cooperative kernel. Its
+"""The small-batch path of moe_forward: for T <= 4096 (dropless, one slot per expert, router on the CUDA
+cores: E < 128 or not a multiple of 32) the router, top-k, counts, offsets, rows and the dispatch copy
+run as one cooperative kernel. Its
 results must be bit for bit those of the step entry points (moe_route + moe_dispatch, the six
 standalone kernels), and the step must launch fewer kernels. The layer outputs of these shapes are
 checked against the oracle in test_gpu_parity.py and test_gpu_fullsize.py."""
@@ -15,20 +16,20 @@ pytestmark = pytest.mark.gpu
 
 W = synth.WORKLOADS
 CASES = {
-    # CUDA-core router fused (E = 8), the largest fused batch
+    # E = 8, the largest fused batch
     "tiny": W["tiny"],
     # one token; E = 64 (one router expert block of 64), shared expert on the side stream
     "one_token": W["dsv3_prefill"].replace(name="one_token", T=1, h=256, E=64, I=128, I_shared=128),
-    # tensor-core router (E = 256) before the fused top-k + dispatch, shared expert on the side stream
-    "e256": W["dsv3_prefill"].replace(name="e256", T=300, h=512, E=256, I=128, I_shared=128),
-    # E = 96: CUDA-core router with two expert blocks
+    # E = 96: two router expert blocks (64 + 32), k = 6
     "e96": W["mixtral"].replace(name="e96", T=777, h=512, E=96, k=6, I=128),
+    # E = 40 (not a multiple of 32): CUDA-core router with a partial lane group in the top-k
+    "e40": W["dsv3_prefill"].replace(name="e40", T=333, h=256, E=40, k=4, n_group=4, topk_group=2, I=128,
+                                     I_shared=128),
     # FP8: the shared expert's rows are quantised by the fused copy
     "fp8": W["dsv3_fp8"].replace(name="fp8_fused", T=300, h=512, E=64, I=256, I_shared=256),
     # NVFP4 weights: bf16 copy, shared rows included
-    "fp4": W["dsv3_decode_fp4"].replace(name="fp4_fused", T=130, h=256, E=256, I=256, I_shared=256),
+    "fp4": W["dsv3_decode_fp4"].replace(name="fp4_fused", T=130, h=256, E=64, I=256, I_shared=256),
 }
-
 
 @pytest.fixture(scope="module", autouse=True)
 def built():
