@@ -73,28 +73,53 @@ def layer_counts(wl, active_experts):
     return flops, gemm_flops, bytes_
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_fp8.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh")
+# the sources each grouped-GEMM kernel is compiled from (a DRAM capture is valid while they are unchanged)
+GEMM_KERNEL_SOURCES = {
+    "grouped_gemm_bf16_kernel": ("gemm.cu", "gemm_common.cuh", "common.cuh"),
+    "grouped_gemm_bf16_pair_kernel": ("gemm_pair.cu", "gemm_common.cuh", "common.cuh"),
+    "grouped_gemm_fp8_kernel": ("gemm_fp8.cu", "gemm_common.cuh", "common.cuh"),
+    "grouped_gemm_nvfp4_kernel": ("gemm_fp4.cu", "gemm_common.cuh", "common.cuh"),
+}
 
 
-def gemm_source_sha():
-    """sha256 over the sources the grouped-GEMM kernels are compiled from."""
+def gemm_source_sha(kernel):
+    """sha256 over the sources one grouped-GEMM kernel is compiled from."""
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in GEMM_KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(ROOT, "routing_dispatch_expert_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 
 
-def gemm_traffic_from_profile(wl):
-    """DRAM bytes per expert-GEMM launch (mean of the gate/up and down launches) from the committed
-    ncu summary, if it was taken on the current kernel sources and this workload; else None."""
+def gemm_split_bytes(wl, active_experts):
+    """Algorithmic bytes of the gate/up and of the down launch of moe_expert_ffn (the shared expert, if
+    any, as one more group): the weights of the experts with rows (and the shared expert's) read once,
+    the expert-major rows read, the SwiGLU product written (gate/up) and read back (down), the expert
+    outputs written (down)."""
+    R_tot = wl.T * wl.k + (wl.T if wl.has_shared else 0)
+    act = 1.0 if wl.dtype == "fp8" else 2.0
+    wb = weight_bytes(wl)
+    groups = active_experts + (1 if wl.has_shared else 0)
+    gate_up = groups * 2.0 * wl.I * wl.h * wb + R_tot * wl.h * act + R_tot * wl.I * act
+    down = groups * 1.0 * wl.h * wl.I * wb + R_tot * wl.I * act + R_tot * wl.h * 2.0
+    return gate_up, down
+
+
+def gemm_traffic_from_profile(wl, active_experts):
+    """DRAM bytes per expert-GEMM launch (mean of the gate/up and down launches) of this workload, from
+    the committed ncu summary: the two launches were captured on a small case of the same kernel (a few
+    GB on the device), and their measured bytes are scaled to the full workload by the ratio of the full
+    to the small case's algorithmic bytes (the traffic grows with the weights of the active experts and
+    the rows, which is what the algorithmic bytes count). None if the capture was not taken on the
+    current sources of its kernel or has no entry for this workload."""
     p = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("kernel_source_sha256") != gemm_source_sha():
-        return None
     entry = d.get("workloads", {}).get(wl.name)
-    return entry.get("dram_bytes_per_launch") if entry else None
+    if not entry or entry.get("kernel_source_sha256") != gemm_source_sha(entry["kernel"]):
+        return None
+    ratio = sum(entry["measured_bytes"]) / sum(entry["small_case_algorithmic_bytes"])
+    return ratio * sum(gemm_split_bytes(wl, active_experts)) / 2.0
 
 
 class ClockSampler:
@@ -583,7 +608,7 @@ def measure(wl, args, dev, dist, rde, synth, torch, steps, gpu_index, sustain_s=
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     gemm_peak = peaks["bf16_tflops"] * ratio
     gemm_peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
-    traffic = gemm_traffic_from_profile(wl)
+    traffic = gemm_traffic_from_profile(wl, active)
     hbm_bound = t_compute < bytes_ / p_hbm
     if wl.dtype == "fp8":
         gemm_kernel = "grouped_gemm_fp8_kernel"
@@ -731,7 +756,7 @@ def main():
             "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if wl.dtype == "fp8" else "bf16",
-            "data": "synthetic", "config": config_of(wl, world),
+            "data": "synthetic", "config": dict(config_of(wl, world), l2=head["l2"]),
         }
         for key in ("roofline", "layer_roofline", "balance", "ms_moe_forward", "ms_split_step", "ms_expert_ffn",
                     "graph", "e2e", "gpu_launches", "clocks", "sustained"):

@@ -40,7 +40,9 @@ constexpr int QC_BYTES = BN * BK / 2;  // codes: 256 rows x 32 bytes
 constexpr int QS_BYTES = BN * 16;      // scales: 256 rows x 16 bytes (the scales of 4 K blocks)
 constexpr int Q_BYTES = QC_BYTES + QS_BYTES;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int CONV_WARPS = 8;
+constexpr int CONV_GROUP_WARPS = 8;  // one converter group: one weight row per thread (256 rows)
+constexpr int CONV_GROUPS = 2;       // groups take alternate K blocks, so two stages expand at once
+constexpr int CONV_WARPS = CONV_GROUP_WARPS * CONV_GROUPS;
 constexpr int THREADS = 32 * (6 + CONV_WARPS);
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = STAGES * (A_BYTES + Q_BYTES) + BSTAGES * B_BYTES + 1024;
@@ -104,10 +106,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(&s.afull[i], 1);
         mbar_init(&s.aempty[i], 1);
         mbar_init(&s.qfull[i], 1);
-        mbar_init(&s.qempty[i], CONV_WARPS);
+        mbar_init(&s.qempty[i], CONV_GROUP_WARPS);
       }
       for (int i = 0; i < BSTAGES; ++i) {
-        mbar_init(&s.bfull[i], CONV_WARPS);
+        mbar_init(&s.bfull[i], CONV_GROUP_WARPS);
         mbar_init(&s.bempty[i], 1);
       }
       for (int i = 0; i < 2; ++i) {
@@ -224,13 +226,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     umma_commit(&s.mma_done);
     grp::drain_wait(&s.mma_done, 0, args.wait_limit);
   } else if (warp >= 6) {
-    // ---------------- weight expansion: FP4 row -> 64 bf16 in the swizzled operand layout
-    const int n = threadIdx.x - 6 * 32;  // weight-tile row, 0..255
+    // ---------------- weight expansion: FP4 row -> 64 bf16 in the swizzled operand layout. Each group
+    // of eight warps expands every other K block (group g the blocks i with i % 2 == g), so one
+    // group's loads, conversions, stores and proxy fence of a stage overlap the other group's.
+    const int cw = warp - 6;
+    const int cgroup = cw / CONV_GROUP_WARPS;
+    const int n = (cw % CONV_GROUP_WARPS) * 32 + lane;  // weight-tile row, 0..255
     int stage = 0, bst = 0;
     uint32_t phase = 0, bphase = 0;
     bool fine = true;
+    long long seen = 0;  // K blocks of this CTA so far
     for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < kblocks; ++kb, ++seen) {
+        if ((int)(seen % CONV_GROUPS) != cgroup) {
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++bst == BSTAGES) {
+            bst = 0;
+            bphase ^= 1;
+          }
+          continue;
+        }
         // every lane polls the barriers itself (cheaper than a lane-0 wait and a broadcast)
         const int ok = wait_or_abort(&s.qfull[stage], phase, &s.abort_flag, args.status, args.wait_limit) &&
                        wait_or_abort(&s.bempty[bst], bphase ^ 1, &s.abort_flag, args.status, args.wait_limit);
