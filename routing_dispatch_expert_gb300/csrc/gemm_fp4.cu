@@ -14,11 +14,12 @@
 // multiplies the accumulator in the epilogue. (The block-scaled FP4 MMA would need FP4 activations as
 // well.)
 //
-// Roles, 448 threads: warp 0 lane 0 TMA producer (activation tile, weight codes and scales), warp 1
-// lane 0 MMA issuer, warps 2-5 epilogue, warps 6-13 expand the weight tile (one row per thread: 32
-// bytes of codes and 4 scale bytes -> 64 bf16 written in the 128-byte-swizzled K-major layout the MMA
-// reads). Rings: activations 4 x 16 KB, FP4 tiles 4 x 12 KB, bf16 weight tiles 3 x 32 KB. Every wait
-// is bounded; a time-out records MOE_STATUS_WAIT_TIMEOUT and every role returns.
+// Roles, 704 threads: warp 0 lane 0 TMA producer (activation tile, weight codes and scales), warp 1
+// lane 0 MMA issuer, warps 2-5 epilogue, warps 6-21 expand the weight tile in two groups of eight that
+// take alternate K blocks (within a group one row per thread: 32 bytes of codes and 4 scale bytes -> 64
+// bf16 written in the 128-byte-swizzled K-major layout the MMA reads). Rings: activations 4 x 16 KB,
+// FP4 tiles 4 x 12 KB, bf16 weight tiles 3 x 32 KB. Every wait is bounded; a time-out records
+// MOE_STATUS_WAIT_TIMEOUT and every role returns.
 #include <cuda.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
