@@ -3,7 +3,7 @@ the bench times (moe_forward): full routing and permutation bit-exact, sampled d
 bit-exact, the router GEMM of every token within its derived error bound, and the expert rows,
 shared-expert rows and layer outputs of a large token sample within tolerance.
 
-The sample (SURVEY: a seeded sample of at least 2048 tokens for the FFN and combine) holds 2048
+The sample (at least 2048 seeded tokens for the expert FFN and the combine) holds 2048
 seeded random tokens plus forced ones: for every expert with rows, the tokens of the first and last
 row of its last 128-row tile (the ragged tail a grouped GEMM tile covers only partly, which the
 CTA-pair kernel runs as a half tile), and for the four busiest experts 64 tokens spread over their
