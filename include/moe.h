@@ -23,6 +23,9 @@
  *   - bf16 tensors hold IEEE bfloat16 bit patterns; FP8 tensors hold OCP e4m3 codes (uint8).
  *   - Row-major layouts throughout; "[A, B]" means B is the contiguous dimension.
  *   - Results are deterministic: identical inputs give identical bits (no floating-point atomics).
+ *   - A workspace holds one call's intermediates and counters: calls that share a workspace must not
+ *     overlap on the GPU (enqueue them on one stream, or order them with events). Calls with their own
+ *     workspaces may run concurrently, from any host threads and streams.
  *   - Return value: MOE_OK (0) or a negative status; moe_last_error() then describes it. Argument
  *     errors are detected before any work is enqueued.
  *
