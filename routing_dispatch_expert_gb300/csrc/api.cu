@@ -216,11 +216,7 @@ int do_router_gemm(const moe_config* c, const void* x, const moe_weights* w, flo
       e = moe::launch_grouped_gemm_bf16(g, stream, &err);
       if (e != cudaSuccess) return err.empty() ? cuda_fail(e, "router GEMM launch") : cuda_fail(e, err.c_str());
       counted(2);
-      if (g.csplit > 1) {
-        e = moe::launch_router_reduce(partials, logits, g.csplit, (int64_t)c->T * c->E, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "router partial-sum launch");
-        counted(1);
-      }
+      // a split K range leaves partial sums; the top-k adds them (see do_route)
     } else {
       e = moe::launch_router_gemm(x, w->w_router, logits, c->T, c->h, c->E, stream);
       if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
@@ -251,11 +247,19 @@ moe::TopkDesc topk_desc(const moe_config* c, const moe_weights* w, const float* 
 
 int do_route(const moe_config* c, const void* x, const moe_weights* w, float* logits, int flags, int32_t* topk_idx,
              float* topk_w, void* ws, const Layout& L, cudaStream_t stream) {
+  moe::TopkDesc d = topk_desc(c, w, logits, topk_idx, topk_w);
   if (!(flags & MOE_LOGITS_GIVEN)) {
     const int rc = do_router_gemm(c, x, w, logits, ws, L, stream);
     if (rc) return rc;
+    // a tensor-core router whose K range was split over CTAs left partial sums in the scratch region:
+    // the top-k kernel adds them in split order and writes the logits (one launch fewer)
+    const int cs = router_csplit(c);
+    if (tensor_core_router(c) && cs > 1) {
+      d.partials = at<float>(ws, L.l.scratch + scratch_core_bytes(c));
+      d.splits = cs;
+    }
   }
-  cudaError_t e = moe::launch_topk(topk_desc(c, w, logits, topk_idx, topk_w), stream);
+  cudaError_t e = moe::launch_topk(d, stream);
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   if (c->T > 0) counted(1);
   return MOE_OK;

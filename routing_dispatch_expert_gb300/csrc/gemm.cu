@@ -17,7 +17,7 @@
 //           320-thread instantiation: 256-column tiles drained by eight epilogue warps (two per
 //           TMEM lane quarter), or 128-column tiles by four when the K range is split. A batch
 //           too small to fill the SMs splits each tile's K range over `csplit` CTAs, which write fp32
-//           partial sums that launch_router_reduce adds in split order.
+//           partial sums that the top-k kernel adds in split order.
 // Work follows the device-side per-expert counts (Perplexity, "Quantization": kernels read the
 // routing information to split the work, instead of sizing it from buffer bounds), so the launch
 // needs no host read-back and has a fixed grid.
@@ -560,24 +560,6 @@ __global__ void wait_timeout_selftest_kernel(int* status, long long limit) {
 
 cudaError_t launch_wait_timeout_selftest(int* status, long long limit_cycles, cudaStream_t stream) {
   wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_cycles);
-  return cudaGetLastError();
-}
-
-// logits[i] = sum over s of partials[s][i], in split order (one thread per output element).
-__global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ partials, float* __restrict__ out,
-                                                            int splits, int64_t n) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    float v = partials[i];
-    for (int q = 1; q < splits; ++q) v = __fadd_rn(v, partials[(int64_t)q * n + i]);
-    out[i] = v;
-  }
-}
-
-cudaError_t launch_router_reduce(const float* partials, float* logits, int splits, int64_t n, cudaStream_t stream) {
-  if (n == 0) return cudaSuccess;
-  int64_t blocks = cdiv(n, 256);
-  if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
-  router_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(partials, logits, splits, n);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,10 @@ struct TopkDesc {
   float* topk_w;
   int T, E, k, n_group, topk_group, score, renorm;
   float routed_scale;
+  // a router GEMM whose K range was split over CTAs leaves `splits` partial sums [splits, T, E]; the
+  // top-k adds them in split order and writes the sums to `logits` (nullptr: logits are given)
+  const float* partials = nullptr;
+  int splits = 1;
 };
 cudaError_t launch_topk(const TopkDesc& d, cudaStream_t stream);
 
@@ -132,8 +136,6 @@ struct GroupedGemmDesc {
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
 // one bounded mbarrier wait that nothing completes: records MOE_STATUS_WAIT_TIMEOUT in *status
 cudaError_t launch_wait_timeout_selftest(int* status, long long limit_cycles, cudaStream_t stream);
-// logits[i] = partials[0][i] + partials[1][i] + ... (split order), i < n
-cudaError_t launch_router_reduce(const float* partials, float* logits, int splits, int64_t n, cudaStream_t stream);
 // The expert FFN projections (modes 0 and 1) on CTA pairs: 256 x 256 tiles, tcgen05.mma.cta_group::2.
 cudaError_t launch_grouped_gemm_bf16_pair(const GroupedGemmDesc& d, cudaStream_t stream, std::string* err);
 

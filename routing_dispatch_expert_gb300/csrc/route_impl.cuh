@@ -300,7 +300,23 @@ __device__ __forceinline__ void topk_token(const TopkDesc& d, const Slots<EPL>& 
   const bool vec = EPL % 4 == 0 && d.E == 32 * EPL && (reinterpret_cast<uintptr_t>(d.logits) & 15) == 0;
   const float* lrow = d.logits + (int64_t)t * d.E;
   float key[EPL], lv[EPL];
-  if (vec) {
+  if (d.partials) {
+    // the router's split-K partial sums, added in split order (as the separate reduction would) and
+    // stored as the logits
+    const int64_t n = (int64_t)d.T * d.E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane * EPL + i;
+      float v = 0.f;
+      if (sl.valid[i]) {
+        const float* p = d.partials + (int64_t)t * d.E + e;
+        v = p[0];
+        for (int q = 1; q < d.splits; ++q) v = __fadd_rn(v, p[(int64_t)q * n]);
+        const_cast<float*>(d.logits)[(int64_t)t * d.E + e] = v;
+      }
+      lv[i] = v;
+    }
+  } else if (vec) {
 #pragma unroll
     for (int i = 0; i < EPL; i += 4) {
       const float4 q = *reinterpret_cast<const float4*>(lrow + lane * EPL + i);
