@@ -316,11 +316,15 @@ def reference_arm(args, wl, rank, world):
     print(json.dumps(line), flush=True)
 
 
+L2_FLUSHED = "flushed between steps (a buffer of 4 x L2 overwritten outside the timed events)"
+L2_LARGER = "inputs larger than L2: every step reads all active expert weights (GBs) once"
+
+
 def config_of(wl, world):
     return {"workload": wl.name, "T": wl.T, "h": wl.h, "E": wl.E, "k": wl.k, "I": wl.I, "I_shared": wl.I_shared,
             "n_group": wl.n_group, "topk_group": wl.topk_group, "score": wl.score, "expert_dtype": wl.dtype,
             "zipf_s": wl.zipf_s, "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2: every step reads all active expert weights (GBs) once"}
+            "l2": L2_FLUSHED if fits_in_l2(wl) else L2_LARGER}
 
 
 def measure_fp8_peak(n=8192, sustain_s=4.0):
@@ -408,7 +412,7 @@ def make_layer(wl, dev, rde, synth, torch):
     return cfg, weights, ws, inp["x"]
 
 
-def fits_in_l2(wl, props):
+def fits_in_l2(wl, props=None):
     """True when a step's weights and activations could stay in L2 between steps (then L2 is flushed)."""
     w = 3.0 * wl.h * wl.I * (wl.E + (1 if wl.has_shared else 0)) * weight_bytes(wl)
     return w + 4.0 * wl.T * wl.h < 2 * getattr(props, "L2_cache_size", 129 << 20)
@@ -637,8 +641,7 @@ def measure(wl, args, dev, dist, rde, synth, torch, steps, gpu_index, sustain_s=
     out = {
         "workload": wl.name, "steps": steps, "ms_per_step": ms_step, "value": job_tokens_per_s(world, wl.T, ms_step),
         "unit": UNIT,
-        "l2": ("flushed between steps (a buffer of 4 x L2 overwritten outside the timed events)" if flush is not None
-               else "inputs larger than L2: every step reads all active expert weights (GBs) once"),
+        "l2": L2_FLUSHED if flush is not None else L2_LARGER,
         "roofline": roof,
         "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3), "flops": flops,
                            "bytes": bytes_, "active_experts": active, "bound": "hbm" if hbm_bound else "tensor",
@@ -756,7 +759,7 @@ def main():
             "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if wl.dtype == "fp8" else "bf16",
-            "data": "synthetic", "config": dict(config_of(wl, world), l2=head["l2"]),
+            "data": "synthetic", "config": config_of(wl, world),
         }
         for key in ("roofline", "layer_roofline", "balance", "ms_moe_forward", "ms_split_step", "ms_expert_ffn",
                     "graph", "e2e", "gpu_launches", "clocks", "sustained"):
