@@ -16,8 +16,8 @@
 //
 // Roles, 704 threads: warp 0 lane 0 TMA producer (activation tile, weight codes and scales), warp 1
 // lane 0 MMA issuer, warps 2-5 epilogue, warps 6-21 expand the weight tile in two groups of eight that
-// take alternate K blocks (within a group one row per thread: 32 bytes of codes and 4 scale bytes -> 64
-// bf16 written in the 128-byte-swizzled K-major layout the MMA reads). Rings: activations 4 x 16 KB,
+// take alternate K blocks (within a group two half rows per thread: 16 bytes of codes and 2 scale bytes
+// -> 32 bf16 each, written in the 128-byte-swizzled K-major layout the MMA reads). Rings: activations 4 x 16 KB,
 // FP4 tiles 4 x 12 KB, bf16 weight tiles 3 x 32 KB. Every wait is bounded; a time-out records
 // MOE_STATUS_WAIT_TIMEOUT and every role returns.
 #include <cuda.h>
@@ -232,7 +232,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // group's loads, conversions, stores and proxy fence of a stage overlap the other group's.
     const int cw = warp - 6;
     const int cgroup = cw / CONV_GROUP_WARPS;
-    const int n = (cw % CONV_GROUP_WARPS) * 32 + lane;  // weight-tile row, 0..255
+    // thread j of the group takes the half rows (j / 2 + 128 p, half j % 2), p = 0, 1: a warp's code
+    // loads are then 512 consecutive bytes (no bank conflicts on the 32-byte rows of the FP4 tile)
+    const int j = (cw % CONV_GROUP_WARPS) * 32 + lane;
+    const int hh = j & 1;
     int stage = 0, bst = 0;
     uint32_t phase = 0, bphase = 0;
     bool fine = true;
@@ -259,23 +262,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         const uint8_t* q = ring_q + stage * Q_BYTES;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(q + n * 32);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(q + n * 32 + 16);
-        const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(q + QC_BYTES + n * 16 + (kb & 3) * 4);
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint8_t* brow = ring_b + bst * B_BYTES + n * 128;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const __half_raw sr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sc4 >> (8 * b)) & 0xFF), __NV_E4M3);
-          const __half sh = *reinterpret_cast<const __half*>(&sr);
-          const __half2 s2 = __halves2half2(sh, sh);
+        for (int p = 0; p < 2; ++p) {
+          const int n = (j >> 1) + 128 * p;  // weight-tile row
+          const uint4 cv = *reinterpret_cast<const uint4*>(q + n * 32 + hh * 16);
+          const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(q + QC_BYTES + n * 16 + (kb & 3) * 4 + hh * 2);
+          const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
+          uint8_t* brow = ring_b + bst * B_BYTES + n * 128;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 2 * b + h;
-            const uint32_t w = words[c];
-            const uint4 o = make_uint4(expand2(w & 0xFF, s2), expand2((w >> 8) & 0xFF, s2),
-                                       expand2((w >> 16) & 0xFF, s2), expand2(w >> 24, s2));
-            *reinterpret_cast<uint4*>(brow + ((c ^ (n & 7)) << 4)) = o;
+          for (int b = 0; b < 2; ++b) {
+            const __half_raw sr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sc2 >> (8 * b)) & 0xFF), __NV_E4M3);
+            const __half sh = *reinterpret_cast<const __half*>(&sr);
+            const __half2 s2 = __halves2half2(sh, sh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = 4 * hh + 2 * b + h;  // 16-byte chunk of the row: 8 elements
+              const uint32_t w = words[2 * b + h];
+              const uint4 o = make_uint4(expand2(w & 0xFF, s2), expand2((w >> 8) & 0xFF, s2),
+                                         expand2((w >> 16) & 0xFF, s2), expand2(w >> 24, s2));
+              *reinterpret_cast<uint4*>(brow + ((c ^ (n & 7)) << 4)) = o;
+            }
           }
         }
         fence_proxy_async_smem();  // the tensor core reads this tile through the async proxy
