@@ -301,21 +301,24 @@ __device__ __forceinline__ void topk_token(const TopkDesc& d, const Slots<EPL>& 
   const float* lrow = d.logits + (int64_t)t * d.E;
   float key[EPL], lv[EPL];
   if (d.partials) {
-    // the router's split-K partial sums, added in split order (as the separate reduction would) and
-    // stored as the logits
+    // the router's split-K partial sums, added in split order and stored as the logits; the loads of
+    // one split for all of a lane's experts (and, unrolled, of the next splits) are independent, so
+    // they are in flight together
     const int64_t n = (int64_t)d.T * d.E;
+    const float* p = d.partials + (int64_t)t * d.E + lane * EPL;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane * EPL + i;
-      float v = 0.f;
-      if (sl.valid[i]) {
-        const float* p = d.partials + (int64_t)t * d.E + e;
-        v = p[0];
-        for (int q = 1; q < d.splits; ++q) v = __fadd_rn(v, p[(int64_t)q * n]);
-        const_cast<float*>(d.logits)[(int64_t)t * d.E + e] = v;
-      }
-      lv[i] = v;
+    for (int i = 0; i < EPL; ++i) lv[i] = sl.valid[i] ? p[i] : 0.f;
+#pragma unroll 4
+    for (int q = 1; q < d.splits; ++q) {
+      float vq[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) vq[i] = sl.valid[i] ? p[(int64_t)q * n + i] : 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) lv[i] = __fadd_rn(lv[i], vq[i]);
     }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (sl.valid[i]) const_cast<float*>(d.logits)[(int64_t)t * d.E + lane * EPL + i] = lv[i];
   } else if (vec) {
 #pragma unroll
     for (int i = 0; i < EPL; i += 4) {
