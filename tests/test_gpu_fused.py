@@ -25,6 +25,10 @@ CASES = {
     # E = 40 (not a multiple of 32): CUDA-core router with a partial lane group in the top-k
     "e40": W["dsv3_prefill"].replace(name="e40", T=333, h=256, E=40, k=4, n_group=4, topk_group=2, I=128,
                                      I_shared=128),
+    # E = 200 (not a multiple of 32): four router expert blocks of 64 in the fused router phase, a partial
+    # lane group in the top-k, sigmoid scoring without groups
+    "e200": W["dsv3_prefill"].replace(name="e200", T=512, h=256, E=200, k=6, n_group=1, topk_group=1, I=128,
+                                      I_shared=0),
     # FP8: the shared expert's rows are quantised by the fused copy
     "fp8": W["dsv3_fp8"].replace(name="fp8_fused", T=300, h=512, E=64, I=256, I_shared=256),
     # NVFP4 weights: bf16 copy, shared rows included

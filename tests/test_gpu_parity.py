@@ -26,6 +26,9 @@ SMALL = {
     # E >= 128: the router GEMM runs on the tensor cores (fp32 weight as three bf16 terms)
     "dsv3_e256": _W["dsv3_prefill"].replace(name="dsv3_e256", T=300, h=512, E=256, I=128, I_shared=128),
     "dsv3_e128_skew": _W["dsv3_decode"].replace(name="dsv3_e128_skew", T=130, h=256, E=128, I=128, I_shared=128),
+    # E = 200 (not a multiple of 32): CUDA-core router with four expert blocks, fused small-batch path
+    "e200_fused": _W["dsv3_prefill"].replace(name="e200_fused", T=512, h=256, E=200, k=6, n_group=1, topk_group=1,
+                                             I=128, I_shared=0),
     # the FP8 layer: e4m3 experts with 128x128 scales, 1x128 activations, SiLU output requantised
     "fp8_small": _W["dsv3_fp8"].replace(name="fp8_small", T=300, h=512, E=64, I=256, I_shared=256),
     "fp8_e256_skew": _W["dsv3_fp8"].replace(name="fp8_e256_skew", T=257, h=256, E=256, I=128, I_shared=128),
