@@ -309,9 +309,16 @@ int do_dispatch(const moe_config* c, const void* x, const int32_t* topk_idx, con
 // only five short launches, and measured slower than them (a 256-token decode step: about 46 us
 // against about 30 us, its phases separated by grid barriers and its top-k latency-bound on the few
 // tokens). Dropless layers with one slot per expert only.
+// The fused kernel runs on one CTA per SM (16 warps each), so it pays only while the work is small: a
+// router of at most 2^25 multiply-adds (the tiny layer's 4096 x 512 x 8 is 2^24) and a dispatch copy of
+// at most 2^22 elements per copy of x. Beyond that the standalone kernels, with many more warps to
+// hide latency, are faster (a 4096-token layer with h 7168 and 32 experts: 369 us fused under ncu).
+constexpr int64_t kFusedMaxRouterMacs = int64_t(1) << 25;
+constexpr int64_t kFusedMaxRowElems = int64_t(1) << 22;
 bool use_fused(const moe_config* c) {
+  const int64_t th = (int64_t)c->T * c->h;
   return moe::fused_route_dispatch_supported(c->T, c->E) && capacity_of(c) == 0 && !c->placement &&
-         !tensor_core_router(c);
+         !tensor_core_router(c) && th * c->E <= kFusedMaxRouterMacs && th <= kFusedMaxRowElems;
 }
 
 int do_fused_route_dispatch(const moe_config* c, const void* x, const moe_weights* w, void* ws, const Layout& L,

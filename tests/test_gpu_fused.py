@@ -21,7 +21,7 @@ CASES = {
     # one token; E = 64 (one router expert block of 64), shared expert on the side stream
     "one_token": W["dsv3_prefill"].replace(name="one_token", T=1, h=256, E=64, I=128, I_shared=128),
     # E = 96: two router expert blocks (64 + 32), k = 6
-    "e96": W["mixtral"].replace(name="e96", T=777, h=512, E=96, k=6, I=128),
+    "e96": W["mixtral"].replace(name="e96", T=600, h=256, E=96, k=6, I=128),
     # E = 40 (not a multiple of 32): CUDA-core router with a partial lane group in the top-k
     "e40": W["dsv3_prefill"].replace(name="e40", T=333, h=256, E=40, k=4, n_group=4, topk_group=2, I=128,
                                      I_shared=128),
@@ -91,11 +91,13 @@ def test_fused_route_and_dispatch_equal_the_step_entry_points(name):
     assert rde.device_status(cfg, ws) == 0
 
 
-@pytest.mark.parametrize("T,fused", [(1, True), (4096, True), (4097, False)])
-def test_small_batch_step_launches_fewer_kernels(T, fused):
+@pytest.mark.parametrize("T,h,fused", [(1, 512, True), (4096, 512, True), (4097, 512, False), (2048, 4096, False)])
+def test_small_batch_step_launches_fewer_kernels(T, h, fused):
     """The tiny layer (E 8, no shared expert): fused, a step is 4 launches (route-and-dispatch, gate/up,
-    down, combine) instead of 9 (router, top-k, histogram, scan, rank, copy, gate/up, down, combine)."""
-    wl = W["tiny"].replace(T=T)
+    down, combine) instead of 9 (router, top-k, histogram, scan, rank, copy, gate/up, down, combine).
+    Above 4096 tokens, or with more router and copy work than the fused kernel pays for (here h 4096), the standalone
+    kernels run."""
+    wl = W["tiny"].replace(T=T, h=h)
     L = GpuLayer(wl)
     L.forward()
     n0 = rde.launch_count()
