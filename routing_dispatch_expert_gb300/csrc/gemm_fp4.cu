@@ -14,12 +14,14 @@
 // multiplies the accumulator in the epilogue. (The block-scaled FP4 MMA would need FP4 activations as
 // well.)
 //
-// Roles, 704 threads: warp 0 lane 0 TMA producer (activation tile, weight codes and scales), warp 1
-// lane 0 MMA issuer, warps 2-5 epilogue, warps 6-21 expand the weight tile in two groups of eight that
-// take alternate K blocks (within a group two half rows per thread: 16 bytes of codes and 2 scale bytes
-// -> 32 bf16 each, written in the 128-byte-swizzled K-major layout the MMA reads). Rings: activations 4 x 16 KB,
-// FP4 tiles 4 x 12 KB, bf16 weight tiles 3 x 32 KB. Every wait is bounded; a time-out records
-// MOE_STATUS_WAIT_TIMEOUT and every role returns.
+// Roles, 736 threads: warp 0 lane 0 TMA producer of the weight codes and scales, warp 6 lane 0 TMA
+// producer of the activation tiles, warp 1 lane 0 MMA issuer, warps 2-5 epilogue, warps 7-22 expand
+// the weight tile in two groups of eight that take alternate K blocks (within a group two half rows
+// per thread: 16 bytes of codes and 2 scale bytes -> 32 bf16 each, written in the 128-byte-swizzled
+// K-major layout the MMA reads). Rings: activations 3 x 16 KB, FP4 tiles 6 x 12 KB, bf16 weight tiles
+// 3 x 32 KB. The FP4 ring waits only on the converters, so the weight stream runs ahead of the MMA
+// (with one producer for both rings, an FP4 load waited for the MMA to free the activation stage it
+// shared). Every wait is bounded; a time-out records MOE_STATUS_WAIT_TIMEOUT and every role returns.
 #include <cuda.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -34,7 +36,8 @@ namespace g4 {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;   // activation and FP4 weight rings
+constexpr int STAGES = 3;   // activation ring
+constexpr int QSTAGES = 6;  // FP4 weight ring (codes and scales)
 constexpr int BSTAGES = 3;  // expanded bf16 weight ring
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int QC_BYTES = BN * BK / 2;  // codes: 256 rows x 32 bytes
@@ -44,9 +47,10 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int CONV_GROUP_WARPS = 8;  // one converter group: one weight row per thread (256 rows)
 constexpr int CONV_GROUPS = 2;       // groups take alternate K blocks, so two stages expand at once
 constexpr int CONV_WARPS = CONV_GROUP_WARPS * CONV_GROUPS;
-constexpr int THREADS = 32 * (6 + CONV_WARPS);
+constexpr int CONV_WARP0 = 7;  // warps 0-6: FP4 producer, MMA, four epilogue warps, activation producer
+constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int SMEM_BYTES = STAGES * (A_BYTES + Q_BYTES) + BSTAGES * B_BYTES + 1024;
+constexpr int SMEM_BYTES = STAGES * A_BYTES + QSTAGES * Q_BYTES + BSTAGES * B_BYTES + 1024;
 
 struct Args {
   const int32_t* offsets;
@@ -62,7 +66,7 @@ struct Args {
 
 struct Shared {
   uint64_t afull[STAGES], aempty[STAGES];
-  uint64_t qfull[STAGES], qempty[STAGES];
+  uint64_t qfull[QSTAGES], qempty[QSTAGES];
   uint64_t bfull[BSTAGES], bempty[BSTAGES];
   uint64_t tfull[2], tempty[2];
   uint64_t mma_done;
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring_a = smem;
   uint8_t* ring_q = ring_a + STAGES * A_BYTES;
-  uint8_t* ring_b = ring_q + STAGES * Q_BYTES;
+  uint8_t* ring_b = ring_q + QSTAGES * Q_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.E + args.shared;
@@ -106,6 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < STAGES; ++i) {
         mbar_init(&s.afull[i], 1);
         mbar_init(&s.aempty[i], 1);
+      }
+      for (int i = 0; i < QSTAGES; ++i) {
         mbar_init(&s.qfull[i], 1);
         mbar_init(&s.qempty[i], CONV_GROUP_WARPS);
       }
@@ -140,14 +146,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kblocks = args.K / BK;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer: activation tile and the FP4 weight tile of every K block
+    // ---------------- TMA producer of the FP4 weight tiles (codes and scales). Its ring is deeper than
+    // the activation ring and waits only on the converters, so the weight stream runs ahead of the MMA.
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
-      const bool half = t.rows <= BM / 2;  // 64 rows or fewer: a 64-row activation box, an M = 64 MMA
       const bool routed = t.g < args.E;
       const CUtensorMap* mq = routed ? &tmQ : &tmQs;
       const CUtensorMap* ms = routed ? &tmS : &tmSs;
@@ -156,20 +162,43 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int r0 = args.mode == 0 ? t.n_tile * (BN / 2) : t.n_tile * BN;
       const int r1 = args.mode == 0 ? args.I + t.n_tile * (BN / 2) : r0 + BN / 2;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_or_abort(&s.aempty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit) ||
-            !wait_or_abort(&s.qempty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
+        if (!wait_or_abort(&s.qempty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
           break;
         }
-        uint8_t* a = ring_a + stage * A_BYTES;
         uint8_t* q = ring_q + stage * Q_BYTES;
-        mbar_arrive_expect_tx(&s.afull[stage], half ? A_BYTES / 2 : A_BYTES);
-        tma_load_2d(a, half ? &tmA64 : &tmA, &s.afull[stage], kb * BK, t.a_row);
         mbar_arrive_expect_tx(&s.qfull[stage], Q_BYTES);
         tma_load_3d(q, mq, &s.qfull[stage], kb * (BK / 2), r0, z);
         tma_load_3d(q + QC_BYTES / 2, mq, &s.qfull[stage], kb * (BK / 2), r1, z);
         tma_load_3d(q + QC_BYTES, ms, &s.qfull[stage], (kb / 4) * 16, r0, z);
         tma_load_3d(q + QC_BYTES + QS_BYTES / 2, ms, &s.qfull[stage], (kb / 4) * 16, r1, z);
+        ++issued;
+        if (++stage == QSTAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    const long long first = issued > QSTAGES ? issued - QSTAGES : 0;
+    for (long long i = first; i < issued; ++i)
+      grp::drain_wait(&s.qfull[i % QSTAGES], (uint32_t)((i / QSTAGES) & 1), args.wait_limit);
+  } else if (warp == CONV_WARP0 - 1 && lane == 0) {
+    // ---------------- TMA producer of the activation tiles
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
+      const bool half = t.rows <= BM / 2;  // 64 rows or fewer: a 64-row activation box, an M = 64 MMA
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(&s.aempty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = ring_a + stage * A_BYTES;
+        mbar_arrive_expect_tx(&s.afull[stage], half ? A_BYTES / 2 : A_BYTES);
+        tma_load_2d(a, half ? &tmA64 : &tmA, &s.afull[stage], kb * BK, t.a_row);
         ++issued;
         if (++stage == STAGES) {
           stage = 0;
@@ -178,10 +207,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     const long long first = issued > STAGES ? issued - STAGES : 0;
-    for (long long i = first; i < issued; ++i) {
+    for (long long i = first; i < issued; ++i)
       grp::drain_wait(&s.afull[i % STAGES], (uint32_t)((i / STAGES) & 1), args.wait_limit);
-      grp::drain_wait(&s.qfull[i % STAGES], (uint32_t)((i / STAGES) & 1), args.wait_limit);
-    }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     const uint32_t idesc_full = idesc_bf16(BM, BN), idesc_half = idesc_bf16(BM / 2, BN);
@@ -226,11 +253,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     umma_commit(&s.mma_done);
     grp::drain_wait(&s.mma_done, 0, args.wait_limit);
-  } else if (warp >= 6) {
+  } else if (warp >= CONV_WARP0) {
     // ---------------- weight expansion: FP4 row -> 64 bf16 in the swizzled operand layout. Each group
     // of eight warps expands every other K block (group g the blocks i with i % 2 == g), so one
     // group's loads, conversions, stores and proxy fence of a stage overlap the other group's.
-    const int cw = warp - 6;
+    const int cw = warp - CONV_WARP0;
     const int cgroup = cw / CONV_GROUP_WARPS;
     // thread j of the group takes the half rows (j / 2 + 128 p, half j % 2), p = 0, 1: a warp's code
     // loads are then 512 consecutive bytes (no bank conflicts on the 32-byte rows of the FP4 tile)
@@ -243,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total && fine; tile += gridDim.x) {
       for (int kb = 0; kb < kblocks; ++kb, ++seen) {
         if ((int)(seen % CONV_GROUPS) != cgroup) {
-          if (++stage == STAGES) {
+          if (++stage == QSTAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -290,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive(&s.bfull[bst]);
           mbar_arrive(&s.qempty[stage]);
         }
-        if (++stage == STAGES) {
+        if (++stage == QSTAGES) {
           stage = 0;
           phase ^= 1;
         }
@@ -300,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < CONV_WARP0 - 1) {
     // ---------------- epilogue: TMEM -> registers -> global, times the matrix scale
     const int quarter = warp & 3;
     int acc = 0;
