@@ -36,9 +36,9 @@ namespace g4 {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 3;   // activation ring
+// K block i uses activation stage i % STAGES and expanded-weight stage i % STAGES, released together
+constexpr int STAGES = 3;   // activation and expanded bf16 weight rings
 constexpr int QSTAGES = 6;  // FP4 weight ring (codes and scales)
-constexpr int BSTAGES = 3;  // expanded bf16 weight ring
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int QC_BYTES = BN * BK / 2;  // codes: 256 rows x 32 bytes
 constexpr int QS_BYTES = BN * 16;      // scales: 256 rows x 16 bytes (the scales of 4 K blocks)
@@ -50,7 +50,7 @@ constexpr int CONV_WARPS = CONV_GROUP_WARPS * CONV_GROUPS;
 constexpr int CONV_WARP0 = 7;  // warps 0-6: FP4 producer, MMA, four epilogue warps, activation producer
 constexpr int THREADS = 32 * (CONV_WARP0 + CONV_WARPS);
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int SMEM_BYTES = STAGES * A_BYTES + QSTAGES * Q_BYTES + BSTAGES * B_BYTES + 1024;
+constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + QSTAGES * Q_BYTES + 1024;
 
 struct Args {
   const int32_t* offsets;
@@ -65,9 +65,10 @@ struct Args {
 };
 
 struct Shared {
-  uint64_t afull[STAGES], aempty[STAGES];
+  // full[i]: the activation tile landed and eight converter warps wrote the weight tile; empty[i]:
+  // the MMAs of the K block that read both finished
+  uint64_t full[STAGES], empty[STAGES];
   uint64_t qfull[QSTAGES], qempty[QSTAGES];
-  uint64_t bfull[BSTAGES], bempty[BSTAGES];
   uint64_t tfull[2], tempty[2];
   uint64_t mma_done;
   uint32_t tmem_slot;
@@ -108,16 +109,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     grp::build_table(s.tb, args.offsets, args.E, args.shared, args.R, args.T, BM, lane);
     if (lane == 0) {
       for (int i = 0; i < STAGES; ++i) {
-        mbar_init(&s.afull[i], 1);
-        mbar_init(&s.aempty[i], 1);
+        mbar_init(&s.full[i], CONV_GROUP_WARPS + 1);  // the converter warps + the activation producer
+        mbar_init(&s.empty[i], 1);
       }
       for (int i = 0; i < QSTAGES; ++i) {
         mbar_init(&s.qfull[i], 1);
         mbar_init(&s.qempty[i], CONV_GROUP_WARPS);
-      }
-      for (int i = 0; i < BSTAGES; ++i) {
-        mbar_init(&s.bfull[i], CONV_GROUP_WARPS);
-        mbar_init(&s.bempty[i], 1);
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
@@ -192,13 +189,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Tile t = grp::decode(s.tb, G, args.n_tiles, tile, BM);
       const bool half = t.rows <= BM / 2;  // 64 rows or fewer: a 64-row activation box, an M = 64 MMA
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_or_abort(&s.aempty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
+        if (!wait_or_abort(&s.empty[stage], phase ^ 1, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
           break;
         }
         uint8_t* a = ring_a + stage * A_BYTES;
-        mbar_arrive_expect_tx(&s.afull[stage], half ? A_BYTES / 2 : A_BYTES);
-        tma_load_2d(a, half ? &tmA64 : &tmA, &s.afull[stage], kb * BK, t.a_row);
+        mbar_arrive_expect_tx(&s.full[stage], half ? A_BYTES / 2 : A_BYTES);
+        tma_load_2d(a, half ? &tmA64 : &tmA, &s.full[stage], kb * BK, t.a_row);
         ++issued;
         if (++stage == STAGES) {
           stage = 0;
@@ -208,12 +205,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     const long long first = issued > STAGES ? issued - STAGES : 0;
     for (long long i = first; i < issued; ++i)
-      grp::drain_wait(&s.afull[i % STAGES], (uint32_t)((i / STAGES) & 1), args.wait_limit);
+      grp::drain_wait(&s.full[i % STAGES], (uint32_t)((i / STAGES) & 1), args.wait_limit);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     const uint32_t idesc_full = idesc_bf16(BM, BN), idesc_half = idesc_bf16(BM / 2, BN);
-    int stage = 0, bst = 0;
-    uint32_t phase = 0, bphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -224,26 +221,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_or_abort(&s.afull[stage], phase, &s.abort_flag, args.status, args.wait_limit) ||
-            !wait_or_abort(&s.bfull[bst], bphase, &s.abort_flag, args.status, args.wait_limit)) {
+        if (!wait_or_abort(&s.full[stage], phase, &s.abort_flag, args.status, args.wait_limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a = smem_u32(ring_a + stage * A_BYTES);
-        const uint32_t b = smem_u32(ring_b + bst * B_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_f16(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), idesc, (kb | kk) != 0);
-        umma_commit(&s.aempty[stage]);
-        umma_commit(&s.bempty[bst]);
+        // one descriptor per operand tile: the K step kk starts 32 bytes further, 2 in the descriptor's
+        // 16-byte address field (a shared-memory address >> 4 stays below 2^14, so nothing carries).
+        // The issuing thread shares its SM sub-partition with converter warps: every instruction
+        // taken out of this loop shortens the K block.
+        const uint64_t da = sw128_kmajor_desc(smem_u32(ring_a + stage * A_BYTES));
+        const uint64_t db = sw128_kmajor_desc(smem_u32(ring_b + stage * B_BYTES));
+        umma_f16(d, da, db, idesc, kb != 0);
+        umma_f16(d, da + 2, db + 2, idesc, 1);
+        umma_f16(d, da + 4, db + 4, idesc, 1);
+        umma_f16(d, da + 6, db + 6, idesc, 1);
+        umma_commit(&s.empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
-        }
-        if (++bst == BSTAGES) {
-          bst = 0;
-          bphase ^= 1;
         }
       }
       if (!ok) break;
@@ -274,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1;
           }
-          if (++bst == BSTAGES) {
+          if (++bst == STAGES) {
             bst = 0;
             bphase ^= 1;
           }
@@ -282,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // every lane polls the barriers itself (cheaper than a lane-0 wait and a broadcast)
         const int ok = wait_or_abort(&s.qfull[stage], phase, &s.abort_flag, args.status, args.wait_limit) &&
-                       wait_or_abort(&s.bempty[bst], bphase ^ 1, &s.abort_flag, args.status, args.wait_limit);
+                       wait_or_abort(&s.empty[bst], bphase ^ 1, &s.abort_flag, args.status, args.wait_limit);
         if (__any_sync(0xffffffffu, !ok)) {
           fine = false;
           break;
@@ -314,14 +310,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();  // the tensor core reads this tile through the async proxy
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&s.bfull[bst]);
+          mbar_arrive(&s.full[bst]);
           mbar_arrive(&s.qempty[stage]);
         }
         if (++stage == QSTAGES) {
           stage = 0;
           phase ^= 1;
         }
-        if (++bst == BSTAGES) {
+        if (++bst == STAGES) {
           bst = 0;
           bphase ^= 1;
         }
