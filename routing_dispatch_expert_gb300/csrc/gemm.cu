@@ -77,6 +77,7 @@ struct Args {
   int n_valid;  // mode 2: output columns that exist (E)
   int rbn;      // mode 2: output tile width, 128 or 256 (256 needs the ROUTER_THREADS instantiation)
   int ldo;      // output row stride in elements
+  int vec32;    // modes 0 and 1: the output rows and column tiles start on 32-byte boundaries
   void* out;
   const float* row_weight;
   int* status;
@@ -343,9 +344,14 @@ __global__ void __launch_bounds__(NT, 1)
             p[i] = pack_bf16x2(h0, h1);
           }
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            if (args.vec32) {  // one full L2 sector per store
+              st_global_v8(out + c, p);
+              st_global_v8(out + c + 16, p + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
         }
       } else {
@@ -361,9 +367,14 @@ __global__ void __launch_bounds__(NT, 1)
           for (int i = 0; i < 16; ++i)
             p[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * w, __uint_as_float(v[2 * i + 1]) * w);
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            if (args.vec32) {  // one full L2 sector per store
+              st_global_v8(out + c, p);
+              st_global_v8(out + c + 16, p + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
         }
       }
@@ -530,6 +541,7 @@ cudaError_t launch_grouped_gemm_bf16(const GroupedGemmDesc& d, cudaStream_t stre
   a.csplit = d.mode == 2 && d.csplit > 1 ? d.csplit : 1;
   a.n_valid = d.N;
   a.ldo = d.ldo;
+  a.vec32 = (reinterpret_cast<uintptr_t>(d.out) & 31) == 0 && ((int64_t)d.ldo * 2) % 32 == 0;
   a.out = d.out;
   a.row_weight = d.row_weight;
   a.status = d.status;

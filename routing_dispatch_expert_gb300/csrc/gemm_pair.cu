@@ -52,16 +52,6 @@
 
 namespace moe {
 
-
-namespace {
-// 32-byte store (st.global.v8.b32): one full L2 sector per lane; the address must be 32-byte aligned
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
-               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-}  // namespace
-
 namespace g2 {
 
 constexpr int BM = 128;                 // rows per CTA
